@@ -1,0 +1,183 @@
+"""ctypes binding of the C ABI (include/fa.h, include/fa_diag.h).
+
+Argument marshalling only: torch tensors supply device memory and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+There is no fallback: if the shared library is missing, every call raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_WORKSPACE = range(6)
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+                4: "FA_ERR_TIMEOUT", 5: "FA_ERR_WORKSPACE"}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s" % (where, STATUS_NAMES.get(status, status)))
+
+
+class FwdTuning(ctypes.Structure):
+    _fields_ = [("rescale_threshold", ctypes.c_float), ("emu_per_16", ctypes.c_int)]
+
+
+_LIB = None
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+_SIGNATURES = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp]),
+    "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
+                       ctypes.POINTER(FwdTuning), _vp]),
+    "fa_fwd_default_tuning": (FwdTuning, []),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _i,
+                    _vp, _sz, _vp]),
+    "fa_get_device_error": (_i, [_vp]),
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_diag_exp2": (_i, [_vp, _vp, _vp, ctypes.c_longlong, _vp]),
+    "fa_diag_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
+}
+
+
+def lib_path():
+    return _build.LIB
+
+
+def load_library(build_if_missing=False):
+    """Loads (optionally builds) the in-tree shared library; raises if absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(_build.LIB):
+        if not build_if_missing:
+            raise RuntimeError("CUDA library %s is not built; run exact_attention_78_gb300.build.build()"
+                               % _build.LIB)
+        _build.build()
+    lib = ctypes.CDLL(_build.LIB)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(status, where):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_bf16(name, t):
+    if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA bfloat16 tensor" % name)
+
+
+def _dims(q, k, cu_seqlens):
+    """(B, Hq, Hkv, Sq, Sk, D) as the C ABI wants them."""
+    if cu_seqlens is None:
+        if q.dim() != 4 or k.dim() != 4:
+            raise ValueError("dense q/k/v are [B, S, H, D]")
+        B, Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[1], k.shape[2]
+    else:
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("packed q/k/v are [total, H, D]")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be a CUDA int32 tensor")
+        B = cu_seqlens.numel() - 1
+        Sq, Hq, D = q.shape
+        Sk, Hkv = k.shape[0], k.shape[1]
+    return B, Hq, Hkv, Sq, Sk, D
+
+
+def fwd(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, rescale_threshold=None,
+        emu_per_16=None, stream=None):
+    """O, LSE = attention(q, k, v).  Dense [B,S,H,D] or packed [total,H,D]."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(n, t)
+    B, Hq, Hkv, Sq, Sk, D = _dims(q, k, cu_seqlens)
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        shape = (Hq, Sq) if cu_seqlens is not None else (B, Hq, Sq)
+        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
+            float(scale), _ptr(cu_seqlens)]
+    if rescale_threshold is None and emu_per_16 is None:
+        st = lib.fa_fwd(*args, _stream(stream))
+    else:
+        t = lib.fa_fwd_default_tuning()
+        if rescale_threshold is not None:
+            t.rescale_threshold = float(rescale_threshold)
+        if emu_per_16 is not None:
+            t.emu_per_16 = int(emu_per_16)
+        st = lib.fa_fwd_ex(*args, ctypes.byref(t), _stream(stream))
+    _check(st, "fa_fwd")
+    return out, lse
+
+
+def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic=False):
+    return int(load_library().fa_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, int(bool(deterministic))))
+
+
+def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, workspace=None, dq=None, dk=None,
+        dv=None, stream=None):
+    """dQ, dK, dV of attention(q, k, v) given O, LSE and dO (dense layout)."""
+    lib = load_library()
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_bf16(n, t)
+    B, Hq, Hkv, Sq, Sk, D = _dims(q, k, None)
+    if scale is None:
+        scale = D ** -0.5
+    need = bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
+                    Hkv, Sq, Sk, D, int(bool(causal)), float(scale), None, int(bool(deterministic)),
+                    _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def get_device_error(stream=None):
+    """Synchronises and returns (and clears) the library's device error status."""
+    return int(load_library().fa_get_device_error(_stream(stream)))
+
+
+def status_string(status):
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def exp2_probe(x, stream=None):
+    """(2^x by the FMA polynomial, 2^x by the hardware unit) for a CUDA float32 tensor."""
+    lib = load_library()
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    ye, yh = torch.empty_like(x), torch.empty_like(x)
+    _check(lib.fa_diag_exp2(_ptr(x), _ptr(ye), _ptr(yh), x.numel(), _stream(stream)), "fa_diag_exp2")
+    return ye, yh
+
+
+def wait_timeout_probe(limit_ns, stream=None):
+    _check(load_library().fa_diag_wait_timeout(int(limit_ns), _stream(stream)), "fa_diag_wait_timeout")

@@ -1,0 +1,266 @@
+// C ABI of the library (include/fa.h, include/fa_diag.h): argument
+// validation, tensor-map construction, device-error plumbing and dispatch to
+// the kernel translation units.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_diag.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kDefaultEmuPer16 = 0;
+constexpr float kDefaultThreshold = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Current device's SM count; FA_ERR_UNSUPPORTED unless it is compute 10.3.
+fa_status device_info(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Shape checks common to both passes.  Packed inputs: Sq == Sk == total.
+fa_status check_shapes(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, const int* cu_seqlens) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0) return FA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (cu_seqlens != nullptr) {
+    if (Sq != Sk) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_INVALID_ARG;
+    if (B > kMaxPackedSeqs) return FA_ERR_UNSUPPORTED;
+  }
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  // token indices must fit the kernels' 32-bit index arithmetic
+  const long long rows_q = cu_seqlens ? (long long)Sq : (long long)B * Sq;
+  const long long rows_k = cu_seqlens ? (long long)Sk : (long long)B * Sk;
+  if (rows_q > INT32_MAX - 512 || rows_k > INT32_MAX - 512) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic) {
+  BwdWorkspace w{};
+  size_t off = 0;
+  w.dq_acc = off;
+  off = align256(off + (size_t)B * Sq * Hq * D * sizeof(float));
+  w.delta = off;
+  off = align256(off + (size_t)B * Hq * Sq * sizeof(float));
+  w.lse2 = off;
+  off = align256(off + (size_t)B * Hq * Sq * sizeof(float));
+  w.tickets = off;
+  if (deterministic) off = align256(off + (size_t)B * Hq * ((Sq + 127) / 128) * sizeof(int));
+  w.total = off;
+  return w;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_fwd_tuning fa_fwd_default_tuning(void) {
+  fa_fwd_tuning t;
+  t.rescale_threshold = kDefaultThreshold;
+  t.emu_per_16 = kDefaultEmuPer16;
+  return t;
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                    int Sq, int Sk, int D, int causal, float scale, const int* cu_seqlens,
+                    const fa_fwd_tuning* t, fa_stream_t stream) {
+  try {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+      return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shapes(B, Hq, Hkv, Sq, Sk, D, scale, cu_seqlens);
+    if (st != FA_OK) return st;
+    fa_fwd_tuning tune = fa_fwd_default_tuning();
+    if (t) {
+      if (!(t->rescale_threshold >= 0.0f && t->rescale_threshold <= 16.0f)) return FA_ERR_INVALID_ARG;
+      tune.rescale_threshold = t->rescale_threshold;
+      if (t->emu_per_16 >= 0) {
+        if (t->emu_per_16 != 0 && t->emu_per_16 != 2 && t->emu_per_16 != 3 && t->emu_per_16 != 4)
+          return FA_ERR_INVALID_ARG;
+        tune.emu_per_16 = t->emu_per_16;
+      }
+    }
+    int num_sms = 0;
+    if ((st = device_info(&num_sms)) != FA_OK) return st;
+    FwdLaunch L{};
+    L.q = q;
+    L.k = k;
+    L.v = v;
+    L.p.o = o;
+    L.p.lse = lse;
+    L.p.cu_seqlens = cu_seqlens;
+    L.p.B = B;
+    L.p.Hq = Hq;
+    L.p.Hkv = Hkv;
+    L.p.Sq = Sq;
+    L.p.Sk = Sk;
+    L.p.group = Hq / Hkv;
+    L.p.scale_log2 = scale * kLog2e;
+    L.p.thr = tune.rescale_threshold;
+    L.p.wait_limit_ns = kDefaultWaitLimitNs;
+    L.D = D;
+    L.causal = causal != 0;
+    L.emu_per_16 = tune.emu_per_16;
+    L.num_sms = num_sms;
+    return launch_fwd(L, reinterpret_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return FA_ERR_CUDA;
+  }
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                 int Sq, int Sk, int D, int causal, float scale, const int* cu_seqlens, fa_stream_t stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, cu_seqlens, nullptr, stream);
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic) {
+  if (check_shapes(B, Hq, Hkv, Sq, Sk, D, 1.0f, nullptr) != FA_OK) return 0;
+  if (deterministic != 0 && deterministic != 1) return 0;
+  return bwd_workspace_layout(B, Hq, Sq, D, deterministic).total;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                 float scale, const int* cu_seqlens, int deterministic, void* workspace,
+                 size_t workspace_bytes, fa_stream_t stream) {
+  try {
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+    for (const void* p : ptrs)
+      if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
+    fa_status st = check_shapes(B, Hq, Hkv, Sq, Sk, D, scale, cu_seqlens);
+    if (st != FA_OK) return st;
+    if (cu_seqlens != nullptr) return FA_ERR_UNSUPPORTED;
+    const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Sq, D, deterministic);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < ws.total)
+      return FA_ERR_WORKSPACE;
+    int num_sms = 0;
+    if ((st = device_info(&num_sms)) != FA_OK) return st;
+    uint8_t* wb = static_cast<uint8_t*>(workspace);
+    BwdLaunch L{};
+    L.q = q;
+    L.k = k;
+    L.v = v;
+    L.p.o = o;
+    L.p.dout = dout;
+    L.p.lse = lse;
+    L.p.dq = dq;
+    L.p.dk = dk;
+    L.p.dv = dv;
+    L.p.dq_acc = reinterpret_cast<float*>(wb + ws.dq_acc);
+    L.p.delta = reinterpret_cast<float*>(wb + ws.delta);
+    L.p.lse2 = reinterpret_cast<float*>(wb + ws.lse2);
+    L.p.tickets = deterministic ? reinterpret_cast<int*>(wb + ws.tickets) : nullptr;
+    L.p.B = B;
+    L.p.Hq = Hq;
+    L.p.Hkv = Hkv;
+    L.p.Sq = Sq;
+    L.p.Sk = Sk;
+    L.p.D = D;
+    L.p.group = Hq / Hkv;
+    L.p.causal = causal;
+    L.p.deterministic = deterministic;
+    L.p.scale = scale;
+    L.p.scale_log2 = scale * kLog2e;
+    L.p.wait_limit_ns = kDefaultWaitLimitNs;
+    L.num_sms = num_sms;
+    return launch_bwd(L, reinterpret_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return FA_ERR_CUDA;
+  }
+}
+
+fa_status fa_get_device_error(fa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  fa_status first = FA_OK;
+  const fa_status all[3] = {fwd_take_device_error(), bwd_take_device_error(), diag_take_device_error()};
+  for (fa_status s : all)
+    if (first == FA_OK && s != FA_OK) first = s;
+  return first;
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_diag_exp2(const float* x, float* y_emu, float* y_hw, long long n, fa_stream_t stream) {
+  if (n < 0) return FA_ERR_INVALID_ARG;
+  if (n > 0 && (!x || !y_emu || !y_hw)) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  int num_sms = 0;
+  fa_status st = device_info(&num_sms);
+  if (st != FA_OK) return st;
+  return launch_diag_exp2(x, y_emu, y_hw, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_diag_wait_timeout(unsigned long long limit_ns, fa_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
+  int num_sms = 0;
+  fa_status st = device_info(&num_sms);
+  if (st != FA_OK) return st;
+  return launch_diag_wait(limit_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,739 @@
+// Forward pass of exact attention on sm_103a: one persistent, warp-specialised
+// kernel per call.
+//
+// Method (FlashAttention-4 pages):
+//   * tiles of 128 query rows and 128 keys; online softmax; the score matrix
+//     lives only in tensor memory ("FlashAttention-4: Algorithm and Kernel
+//     Pipelining Co-Design for Asymmetric Hardware Scaling", fdeinterviews.com
+//     summary, opening paragraph);
+//   * roles: a load warp (TMA into an mbarrier ring), an MMA warp issuing
+//     tcgen05 MMAs into TMEM, softmax warpgroups, and a separate correction
+//     warpgroup that rescales the output and runs the epilogue (same page,
+//     bullet "Pipeline for asynchronous tensor cores"; "FlashAttention-4:
+//     matrix throughput bottlenecks", lecompute.fr, section "Keep tiles moving
+//     without overwriting live data");
+//   * two query tiles per work unit in ping-pong: while one tile's softmax
+//     runs, the tensor cores work on the other tile (same bullet);
+//   * part of the exponentials on the FMA units by a cubic polynomial with
+//     exponent-bit insertion, the rest on the hardware unit (bullet "Software
+//     exponentials");
+//   * lazy rescaling: the running output is rescaled only when the row
+//     maximum grows by more than the threshold (8 log2 units), with the final
+//     division by the row sum taken at the same, possibly stale, maximum
+//     (bullet "Lazy rescaling");
+//   * longest-processing-time-first order of work units for causal masks and
+//     packed variable lengths (paragraph after the bullets).
+//
+// Thread layout (512 threads, 16 warps, one CTA per SM):
+//   warps 0-3   softmax of query tile 0    (192 registers each)
+//   warps 4-7   softmax of query tile 1    (192)
+//   warps 8-11  correction + epilogue      (80)
+//   warp  12    TMA producer (one lane)    (48)
+//   warp  13    TMEM owner + MMA issuer    (48)
+//   warps 14-15 idle                       (48)
+// Register budget: 2*128*192 + 128*80 + 128*48 = 65,536 = 512 threads x 128.
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [0,128)    S of tile 0 (FP32); P of tile 0 (BF16 pairs) in its first 64
+//   [128,256)  S / P of tile 1
+//   [256,256+D)     O of tile 0 (FP32)
+//   [256+D,256+2D)  O of tile 1
+//
+// Shared memory: Q of both tiles, a ring of K/V tiles (each 128 x D BF16 in
+// 64-column chunks with 128-byte swizzle, as TMA writes them and tcgen05
+// reads them), the barriers, per-row statistics handed from the softmax to the
+// correction warpgroup, and the packed-length schedule tables.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+#include "softmax_math.cuh"
+
+namespace fa {
+namespace fwd {
+
+__device__ DeviceError g_err;
+
+constexpr int kThreads = 512;
+constexpr int kBM = 128;      // query rows per tile
+constexpr int kBN = 128;      // keys per block
+constexpr int kPairRows = 2 * kBM;
+
+// Failure sites recorded with FA_ERR_TIMEOUT.
+enum Site { kSiteSoftmaxS = 1, kSiteCorrP, kSiteCorrO, kSiteMmaQ, kSiteMmaKV, kSiteMmaO, kSiteProdQ, kSiteProdKV };
+
+template <int D, bool VARLEN>
+struct Layout {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kBM * D * 2;     // 128 rows x D BF16
+  static constexpr int kChunkBytes = kBM * 128;      // 128 rows x 64 BF16
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kQ = 0;
+  static constexpr int kKV = kQ + 2 * kTileBytes;
+  static constexpr int kBars = kKV + kStages * kTileBytes;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_ready[2], o_full[2]
+  static constexpr int kNumBars = 2 + 2 * kStages + 8;
+  static constexpr int kMisc = kBars + kNumBars * 8;   // tmem slot, abort, warp flags[8]
+  static constexpr int kStats = kMisc + 64;            // scale/l/m/lr: 4 x [2][128] floats
+  static constexpr int kSched = kStats + 4 * 2 * kBM * 4;
+  // packed schedule: start[S], len[S], seq[S], unit prefix [S+1],
+  // pair-group prefix [P+1], header[4]  (ints)
+  static constexpr int kSchedInts = 3 * kMaxPackedSeqs + (kMaxPackedSeqs + 1) + (kMaxPairsPerSeq + 1) + 4;
+  static constexpr int kSchedBytes = VARLEN ? 4 * kSchedInts : 0;
+  static constexpr int kTotal = kSched + kSchedBytes;
+  static constexpr int kDynamic = kTotal + kSmemAlignSlack;
+  static_assert(kDynamic <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
+
+// One work unit: a pair of 128-row query tiles of one (sequence, head).
+struct Unit {
+  int h;          // query head
+  int pair;       // pair index inside the sequence
+  int q_tok0;     // token index (row of the [rows, H, D] view) of the sequence's first query
+  int k_tok0;     // same for keys
+  int seq_q, seq_k;
+  int b;          // batch / sequence index (for LSE addressing)
+  int n;          // KV blocks to visit
+};
+
+// Packed-length schedule tables (shared memory).  Sequences are sorted by
+// length, longest first (ties by index).
+struct PackedSched {
+  int* start;      // [nseq] first token of the i-th longest sequence
+  int* len;        // [nseq] its length
+  int* seq;        // [nseq] its index
+  int* uprefix;    // [nseq+1] non-causal: units before the i-th longest sequence
+  int* gprefix;    // [P+1]   causal: units before pair group k (pair index P-1-k)
+  int* header;     // [0] total units, [1] max pairs P, [2] total tokens, [3] bad input
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ int unit_kv_blocks(int pair, int seq_q, int seq_k) {
+  int kv_end = seq_k;
+  if (CAUSAL) {
+    // the pair's last row (pair*256 + 255) sees keys <= row + (seq_k - seq_q)
+    kv_end = min(seq_k, pair * kPairRows + kPairRows + (seq_k - seq_q));
+  }
+  return kv_end <= 0 ? 0 : (kv_end + kBN - 1) / kBN;
+}
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p, const PackedSched& ps) {
+  Unit w;
+  if (!VARLEN) {
+    const int npairs = (p.Sq + kPairRows - 1) / kPairRows;
+    const int BH = p.B * p.Hq;
+    int bh;
+    if (CAUSAL) {  // longest first: pairs near the end of the sequence first
+      w.pair = npairs - 1 - u / BH;
+      bh = u % BH;
+    } else {       // every pair costs the same: keep a head's pairs together
+      bh = u / npairs;
+      w.pair = u % npairs;
+    }
+    w.b = bh / p.Hq;
+    w.h = bh % p.Hq;
+    w.q_tok0 = w.b * p.Sq;
+    w.k_tok0 = w.b * p.Sk;
+    w.seq_q = p.Sq;
+    w.seq_k = p.Sk;
+  } else {
+    const int nseq = p.B;
+    int i;
+    if (CAUSAL) {
+      // groups of equal pair index, highest first; group k holds pair P-1-k of
+      // every sequence that has it (a prefix of the longest-first order)
+      const int P = ps.header[1];
+      int lo = 0, hi = P - 1;
+      while (lo < hi) {  // last k with gprefix[k] <= u
+        const int mid = (lo + hi + 1) >> 1;
+        if (ps.gprefix[mid] <= u) lo = mid; else hi = mid - 1;
+      }
+      w.pair = P - 1 - lo;
+      const int idx = u - ps.gprefix[lo];
+      i = idx / p.Hq;
+      w.h = idx % p.Hq;
+    } else {
+      int lo = 0, hi = nseq - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ps.uprefix[mid] <= u) lo = mid; else hi = mid - 1;
+      }
+      i = lo;
+      const int rem = u - ps.uprefix[i];
+      const int np = (ps.len[i] + kPairRows - 1) / kPairRows;
+      w.h = rem / np;
+      w.pair = rem % np;
+    }
+    w.b = ps.seq[i];
+    w.q_tok0 = ps.start[i];
+    w.k_tok0 = ps.start[i];
+    w.seq_q = ps.len[i];
+    w.seq_k = ps.len[i];
+  }
+  w.n = unit_kv_blocks<CAUSAL>(w.pair, w.seq_q, w.seq_k);
+  return w;
+}
+
+// Builds the packed-length tables cooperatively (all threads) and returns the
+// number of work units.  Invalid offsets are recorded as FA_ERR_INVALID_ARG
+// and leave the CTA with no work.
+template <bool CAUSAL>
+__device__ int build_packed_sched(const FwdParams& p, PackedSched& ps, uint8_t* base) {
+  const int nseq = p.B;
+  ps.start = reinterpret_cast<int*>(base);
+  ps.len = ps.start + kMaxPackedSeqs;
+  ps.seq = ps.len + kMaxPackedSeqs;
+  ps.uprefix = ps.seq + kMaxPackedSeqs;
+  ps.gprefix = ps.uprefix + kMaxPackedSeqs + 1;
+  ps.header = ps.gprefix + kMaxPairsPerSeq + 1;
+  if (threadIdx.x == 0) ps.header[3] = 0;
+  __syncthreads();
+  // validate: cu[0] == 0, non-decreasing, cu[B] == total, lengths <= limit
+  for (int b = threadIdx.x; b < nseq; b += blockDim.x) {
+    const int s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
+    bool bad = s1 < s0 || (s1 - s0) > kMaxPairsPerSeq * kPairRows;
+    if (b == 0) bad |= s0 != 0;
+    if (b == nseq - 1) bad |= s1 != p.Sq;
+    if (bad) ps.header[3] = 1;
+  }
+  __syncthreads();
+  if (ps.header[3]) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicCAS(&g_err.status, 0, FA_ERR_INVALID_ARG);
+    return 0;
+  }
+  // rank of each sequence in longest-first order (ties by index)
+  for (int b = threadIdx.x; b < nseq; b += blockDim.x) {
+    const int Lb = p.cu_seqlens[b + 1] - p.cu_seqlens[b];
+    int rank = 0;
+    for (int c = 0; c < nseq; ++c) {
+      const int Lc = p.cu_seqlens[c + 1] - p.cu_seqlens[c];
+      rank += (Lc > Lb) || (Lc == Lb && c < b);
+    }
+    ps.start[rank] = p.cu_seqlens[b];
+    ps.len[rank] = Lb;
+    ps.seq[rank] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int i = 0; i < nseq; ++i) {
+      ps.uprefix[i] = acc;
+      acc += ((ps.len[i] + kPairRows - 1) / kPairRows) * p.Hq;
+    }
+    ps.uprefix[nseq] = acc;
+    const int P = nseq ? (ps.len[0] + kPairRows - 1) / kPairRows : 0;
+    // causal groups: pair index P-1-k for k = 0..P-1; members are the
+    // sequences with more than that many pairs (a prefix of the order)
+    int g = 0, members = 0;
+    for (int k = 0; k < P; ++k) {
+      const int pi = P - 1 - k;   // descending, so the member prefix only grows
+      while (members < nseq && (ps.len[members] + kPairRows - 1) / kPairRows > pi) ++members;
+      ps.gprefix[k] = g;
+      g += members * p.Hq;
+    }
+    ps.gprefix[P] = g;
+    ps.header[0] = acc;   // both orders enumerate the same units
+    ps.header[1] = P;
+    ps.header[2] = p.Sq;
+  }
+  __syncthreads();
+  return ps.header[0];
+}
+
+// Shared-memory handles.  Barriers and the abort flag are addressed through
+// 32-bit shared-window addresses to keep the issue warps' register use low.
+template <int D, bool VARLEN>
+struct Shared {
+  using L = Layout<D, VARLEN>;
+  uint8_t* base;    // aligned dynamic shared memory (generic pointer)
+  uint32_t sbase;   // same, shared-window address
+  FA_DEV uint32_t bar(int i) const { return sbase + L::kBars + 8 * i; }
+  FA_DEV uint32_t q_full() const { return bar(0); }
+  FA_DEV uint32_t q_empty() const { return bar(1); }
+  FA_DEV uint32_t kv_full(int s) const { return bar(2 + s); }
+  FA_DEV uint32_t kv_empty(int s) const { return bar(2 + L::kStages + s); }
+  FA_DEV uint32_t s_full(int t) const { return bar(2 + 2 * L::kStages + t); }
+  FA_DEV uint32_t p_ready(int t) const { return bar(4 + 2 * L::kStages + t); }
+  FA_DEV uint32_t o_ready(int t) const { return bar(6 + 2 * L::kStages + t); }
+  FA_DEV uint32_t o_full(int t) const { return bar(8 + 2 * L::kStages + t); }
+  FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
+  FA_DEV uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + L::kMisc); }
+  FA_DEV int* warp_flag() const { return reinterpret_cast<int*>(base + L::kMisc + 8); }   // [2][4]
+  FA_DEV float* st_scale() const { return reinterpret_cast<float*>(base + L::kStats); }   // [2][128]
+  FA_DEV float* st_l() const { return st_scale() + 2 * kBM; }                             // [2][128]
+  FA_DEV float* st_m() const { return st_l() + 2 * kBM; }                                 // [2][128]
+  FA_DEV float* st_lr() const { return st_m() + 2 * kBM; }                                // [2][128]
+};
+
+// ------------------------------------------------------------------ roles --
+
+// Softmax warpgroup of query tile t: one thread per row of the tile.
+template <int D, bool CAUSAL, bool VARLEN, int EMU>
+__device__ void softmax_role(const int t, const Shared<D, VARLEN>& sh, const uint32_t tmem, const FwdParams& p,
+                             const PackedSched& ps, const int total_units) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int wq = warp & 3;
+  const int r_in_tile = wq * 32 + lane;
+  const uint32_t tm_s = tmem + (uint32_t(wq * 32) << 16) + uint32_t(t * kBN);
+  const float sl2 = p.scale_log2;
+  uint32_t sit = 0;
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
+    if (w.n == 0) continue;
+    const int tile_row0 = w.pair * kPairRows + t * kBM;
+    const int row = tile_row0 + r_in_tile;
+    const int diag = w.seq_k - w.seq_q;
+    float m_run = -INFINITY, l_run = 0.0f, lr_run = 0.0f;
+    for (int j = 0; j < w.n; ++j, ++sit) {
+      if (!mbar_wait_bounded(sh.s_full(t), sit & 1, sh.abort(), &g_err, kSiteSoftmaxS, p.wait_limit_ns)) return;
+      tc_fence_after();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + c * 32, r[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_fence(r[c]);
+
+      const int kv0 = j * kBN;
+      const bool need_mask = (kv0 + kBN > w.seq_k) || (CAUSAL && kv0 + kBN - 1 > tile_row0 + diag);
+      if (need_mask) {
+        int lim = w.seq_k - kv0;                       // columns >= lim are masked
+        if (CAUSAL) lim = min(lim, row + diag - kv0 + 1);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) r[c / 32][c % 32] = __float_as_uint(-INFINITY);
+      }
+      // row maximum of the raw scores (scale > 0)
+      float mx[8];   // mx[i] covers columns [16 i, 16 i + 16)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(r[i / 2][(i % 2) * 16]);
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if ((c % 16) != 0) mx[c / 16] = fmaxf(mx[c / 16], __uint_as_float(r[c / 32][c % 32]));
+      const float m_blk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      // lazy rescaling: move the running maximum only when it grows by more
+      // than the threshold; otherwise keep the stale one (weights <= 2^thr)
+      float factor = 1.0f;
+      bool rescaled = false;
+      if (j == 0) {
+        m_run = m_blk;
+      } else if (m_blk - m_run > p.thr) {   // false for m_blk = -inf
+        factor = ex2_mufu(m_run - m_blk);    // 0 when m_run = -inf
+        m_run = m_blk;
+        rescaled = true;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+      // Two row sums: of the FP32 weights (for the log-sum-exp) and of the
+      // BF16-rounded weights the PV product actually multiplies V by (for the
+      // final division, so the weights used sum to one; under a stale maximum
+      // the largest weight is not 1 and not exact in BF16).
+      float se[2] = {0.f, 0.f}, sr[2] = {0.f, 0.f};
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float x0 = fmaf(__uint_as_float(r[c / 32][c % 32]), sl2, -m_use);
+        const float x1 = fmaf(__uint_as_float(r[(c + 1) / 32][(c + 1) % 32]), sl2, -m_use);
+        const float e0 = exp2_mixed<EMU>(x0, c), e1 = exp2_mixed<EMU>(x1, c + 1);
+        const uint32_t pp = pack_bf16x2(e0, e1);
+        pk[c / 64][(c / 2) % 32] = pp;
+        se[(c / 2) & 1] += e0 + e1;
+        sr[(c / 2) & 1] += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u);
+      }
+      l_run = l_run * factor + (se[0] + se[1]);
+      lr_run = lr_run * factor + (sr[0] + sr[1]);
+      tmem_st32(tm_s + 0, pk[0]);      // P over the first 64 columns of S
+      tmem_st32(tm_s + 32, pk[1]);
+      tmem_st_wait();
+      sh.st_scale()[t * kBM + r_in_tile] = factor;
+      const unsigned any = __any_sync(0xffffffffu, rescaled);
+      if (lane == 0) sh.warp_flag()[t * 4 + wq] = any ? 1 : 0;
+      if (j == w.n - 1) {
+        sh.st_l()[t * kBM + r_in_tile] = l_run;
+        sh.st_lr()[t * kBM + r_in_tile] = lr_run;
+        sh.st_m()[t * kBM + r_in_tile] = m_run;
+      }
+      tc_fence_before();
+      mbar_arrive(sh.p_ready(t));
+    }
+  }
+}
+
+// Correction warpgroup: rescales O rows in TMEM when the softmax moved a
+// row's maximum, and runs the epilogue (O / l in BF16, LSE).
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void correction_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const FwdParams& p,
+                                const PackedSched& ps, const int total_units) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int wq = warp & 3;
+  const int r_in_tile = wq * 32 + lane;
+  const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  const int total_tok = VARLEN ? ps.header[2] : p.B * p.Sq;
+  __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(p.o);
+  uint32_t sit = 0, uit = 0;
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
+    if (w.n > 0) {
+      for (int j = 0; j < w.n; ++j, ++sit) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!mbar_wait_bounded(sh.p_ready(t), sit & 1, sh.abort(), &g_err, kSiteCorrP, p.wait_limit_ns)) return;
+          tc_fence_after();
+          if (j > 0 && sh.warp_flag()[t * 4 + wq]) {
+            const float f = sh.st_scale()[t * kBM + r_in_tile];
+            const uint32_t tm_o = tmem + lane_off + uint32_t(256 + t * D);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tm_o + c * 32, r);
+              tmem_ld_wait();
+              tmem_ld_fence(r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+              tmem_st32(tm_o + c * 32, r);
+            }
+            tmem_st_wait();
+          }
+          tc_fence_before();
+          mbar_arrive(sh.o_ready(t));
+        }
+      }
+    }
+    // epilogue: O / l in BF16, LSE in natural log
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int row = w.pair * kPairRows + t * kBM + r_in_tile;
+      const bool valid = row < w.seq_q;
+      float l = 0.0f, lr = 0.0f, m = -INFINITY;
+      if (w.n > 0) {
+        if (!mbar_wait_bounded(sh.o_full(t), uit & 1, sh.abort(), &g_err, kSiteCorrO, p.wait_limit_ns)) return;
+        tc_fence_after();
+        l = sh.st_l()[t * kBM + r_in_tile];
+        lr = sh.st_lr()[t * kBM + r_in_tile];
+        m = sh.st_m()[t * kBM + r_in_tile];
+      }
+      const float inv = (lr > 0.0f) ? 1.0f / lr : 0.0f;
+      const size_t tok = size_t(w.q_tok0) + size_t(row);
+      uint4* dst = reinterpret_cast<uint4*>(O + (tok * p.Hq + w.h) * D);
+      const uint32_t tm_o = tmem + lane_off + uint32_t(256 + t * D);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        if (w.n > 0) {
+          tmem_ld32(tm_o + c * 32, r);
+          tmem_ld_wait();
+          tmem_ld_fence(r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (valid) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 q;
+            q.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+            q.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+            q.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+            q.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+            dst[c * 4 + v] = q;
+          }
+        }
+      }
+      if (valid) {
+        const float lse = (l > 0.0f) ? (m + log2f(l)) * 0.693147180559945309f : -INFINITY;
+        const size_t li = VARLEN ? size_t(w.h) * total_tok + tok
+                                 : (size_t(w.b) * p.Hq + w.h) * p.Sq + size_t(row);
+        p.lse[li] = lse;
+      }
+    }
+    if (w.n > 0) {
+      tc_fence_before();
+      ++uit;
+    }
+  }
+}
+
+// MMA issuer (one thread).  Issue order per unit, with tiles a = 0, b = 1:
+//   S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | PV_a(1) S_a(2) ... PV_b(n-1)
+// so that while the softmax of one tile runs, the tensor cores compute the
+// other tile's products.  S_t(j+1) overwrites the TMEM columns holding P_t(j)
+// only after PV_t(j) was issued; tcgen05 MMAs of one thread run in order.
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const FwdParams& p,
+                         const PackedSched& ps, const int total_units) {
+  using L = Layout<D, VARLEN>;
+  constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);
+  constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, false, true);
+  const uint32_t q_base = sh.sbase + L::kQ;
+  const uint32_t kv_base = sh.sbase + L::kKV;
+  uint32_t kv_it = 0, sit = 0, uit = 0;
+
+  // S_t = Q_t K^T : M = 128 rows, N = 128 keys, K = D in steps of 16
+  auto issue_s = [&](int t, int stage) {
+    // descriptors differ only in the start-address field: step them
+    const uint64_t da = sdesc_sw128(q_base + t * L::kTileBytes, 16, 1024);
+    const uint64_t db = sdesc_sw128(kv_base + stage * L::kTileBytes, 16, 1024);
+    const uint32_t d_tmem = tmem + t * kBN;
+#pragma unroll 1
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+      mma_ss(d_tmem, da + off, db + off, kIdS, kk > 0 ? 1u : 0u);
+    }
+  };
+  // O_t (+)= P_t V : M = 128 rows, N = D, K = 128 keys in steps of 16;
+  // P from TMEM (8 columns per 16 keys), V MN-major (64-wide D chunks)
+  auto issue_pv = [&](int t, int stage, bool acc) {
+    const uint64_t db = sdesc_sw128(kv_base + stage * L::kTileBytes, L::kChunkBytes, 1024);
+    const uint32_t d_tmem = tmem + 256 + t * D;
+    const uint32_t a_tmem = tmem + t * kBN;
+#pragma unroll 1
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+      // 16 keys = 16 rows of 128 B = 2048 B further into the V tile
+      mma_ts(d_tmem, a_tmem + kk * 8, db + uint64_t(kk * (2048 >> 4)), kIdPV, (acc || kk > 0) ? 1u : 0u);
+    }
+  };
+  auto wait_kv = [&](uint32_t it) -> bool {
+    const int stage = it % L::kStages;
+    if (!mbar_wait_bounded(sh.kv_full(stage), (it / L::kStages) & 1, sh.abort(), &g_err, kSiteMmaKV,
+                           p.wait_limit_ns))
+      return false;
+    tc_fence_after();
+    return true;
+  };
+
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
+    if (w.n == 0) continue;
+    if (!mbar_wait_bounded(sh.q_full(), uit & 1, sh.abort(), &g_err, kSiteMmaQ, p.wait_limit_ns)) return;
+    tc_fence_after();
+    // prologue: S of both tiles for block 0
+    uint32_t k_it = kv_it++;
+    if (!wait_kv(k_it)) return;
+    issue_s(0, k_it % L::kStages);
+    mma_commit(sh.s_full(0));
+    issue_s(1, k_it % L::kStages);
+    mma_commit(sh.s_full(1));
+    mma_commit(sh.kv_empty(k_it % L::kStages));
+    if (w.n == 1) mma_commit(sh.q_empty());
+    for (int j = 0; j < w.n; ++j, ++sit) {
+      const uint32_t v_it = kv_it++;
+      if (!wait_kv(v_it)) return;
+      const bool more = j + 1 < w.n;
+      if (more) k_it = kv_it++;
+      // tile 0: PV(j), then S(j+1)
+      if (!mbar_wait_bounded(sh.o_ready(0), sit & 1, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return;
+      tc_fence_after();
+      issue_pv(0, v_it % L::kStages, j > 0);
+      if (more) {
+        if (!wait_kv(k_it)) return;
+        issue_s(0, k_it % L::kStages);
+        mma_commit(sh.s_full(0));
+      } else {
+        mma_commit(sh.o_full(0));
+      }
+      // tile 1: PV(j), then S(j+1)
+      if (!mbar_wait_bounded(sh.o_ready(1), sit & 1, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return;
+      tc_fence_after();
+      issue_pv(1, v_it % L::kStages, j > 0);
+      mma_commit(sh.kv_empty(v_it % L::kStages));
+      if (more) {
+        issue_s(1, k_it % L::kStages);
+        mma_commit(sh.s_full(1));
+        mma_commit(sh.kv_empty(k_it % L::kStages));
+        if (j + 1 == w.n - 1) mma_commit(sh.q_empty());
+      } else {
+        mma_commit(sh.o_full(1));
+      }
+    }
+    ++uit;
+  }
+}
+
+// TMA producer (one thread): Q of both tiles once per unit, then K_j, V_j in
+// order through the stage ring.
+template <int D, bool CAUSAL, bool VARLEN>
+__device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq, const CUtensorMap* tk,
+                              const CUtensorMap* tv, const FwdParams& p, const PackedSched& ps,
+                              const int total_units) {
+  using L = Layout<D, VARLEN>;
+  uint32_t kv_it = 0, uit = 0;
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
+    if (w.n == 0) continue;
+    const int hk = w.h / p.group;
+    if (!mbar_wait_bounded(sh.q_empty(), (uit & 1) ^ 1, sh.abort(), &g_err, kSiteProdQ, p.wait_limit_ns)) return;
+    mbar_arrive_expect_tx(sh.q_full(), 2 * L::kTileBytes);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_3d(sh.sbase + L::kQ + t * L::kTileBytes + c * L::kChunkBytes, tq, sh.q_full(), c * 64, w.h,
+                    w.q_tok0 + w.pair * kPairRows + t * kBM);
+    for (int j = 0; j < w.n; ++j) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const int stage = kv_it % L::kStages;
+        if (!mbar_wait_bounded(sh.kv_empty(stage), ((kv_it / L::kStages) & 1) ^ 1, sh.abort(), &g_err,
+                               kSiteProdKV, p.wait_limit_ns))
+          return;
+        mbar_arrive_expect_tx(sh.kv_full(stage), L::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sh.sbase + L::kKV + stage * L::kTileBytes + c * L::kChunkBytes, which ? tv : tk,
+                      sh.kv_full(stage), c * 64, hk, w.k_tok0 + j * kBN);
+        ++kv_it;
+      }
+    }
+    ++uit;
+  }
+}
+
+template <int D, bool CAUSAL, bool VARLEN, int EMU>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = Layout<D, VARLEN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32;
+  Shared<D, VARLEN> sh;
+  sh.base = smem;
+  sh.sbase = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    mbar_init(sh.q_full(), 1);
+    mbar_init(sh.q_empty(), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(sh.kv_full(s), 1);
+      mbar_init(sh.kv_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(sh.s_full(t), 1);
+      mbar_init(sh.p_ready(t), kBM);
+      mbar_init(sh.o_ready(t), kBM);
+      mbar_init(sh.o_full(t), 1);
+    }
+    st_shared(sh.abort(), 0);
+    fence_barrier_init();
+  }
+  if (warp == 12 && (threadIdx.x % 32) == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 13) {
+    tmem_alloc(sh.tmem_slot(), 512);
+    tmem_relinquish();
+  }
+  PackedSched ps{};
+  int total_units;
+  if (VARLEN) {
+    total_units = build_packed_sched<CAUSAL>(p, ps, smem + L::kSched);
+  } else {
+    total_units = ((p.Sq + kPairRows - 1) / kPairRows) * p.B * p.Hq;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sh.tmem_slot();
+
+  if (warp < 8) {
+    reg_alloc<192>();
+    softmax_role<D, CAUSAL, VARLEN, EMU>(warp / 4, sh, tmem, p, ps, total_units);
+  } else if (warp < 12) {
+    reg_dealloc<80>();
+    correction_role<D, CAUSAL, VARLEN>(sh, tmem, p, ps, total_units);
+  } else {
+    reg_dealloc<48>();
+    const int lane = threadIdx.x % 32;
+    if (warp == 12 && lane == 0)
+      producer_role<D, CAUSAL, VARLEN>(sh, &tm_q, &tm_k, &tm_v, p, ps, total_units);
+    else if (warp == 13 && lane == 0)
+      mma_role<D, CAUSAL, VARLEN>(sh, tmem, p, ps, total_units);
+  }
+
+  // After a give-up, let copies and MMAs already in flight land before the
+  // shared and tensor memory they target are released.
+  if (ld_shared_volatile(sh.abort())) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool VARLEN, int EMU>
+fa_status launch_inst(const FwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      cudaStream_t stream) {
+  using Lay = Layout<D, VARLEN>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN, EMU>;
+  static bool attr_done = false;  // per instantiation
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kDynamic) != cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_done = true;
+  }
+  int grid = L.num_sms;
+  if (!VARLEN) {
+    const long long units = (long long)((L.p.Sq + kPairRows - 1) / kPairRows) * L.p.B * L.p.Hq;
+    if (units < grid) grid = (int)units;
+  }
+  if (grid < 1) grid = 1;
+  kern<<<grid, kThreads, Lay::kDynamic, stream>>>(tq, tk, tv, L.p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool CAUSAL, bool VARLEN>
+fa_status launch_emu(const FwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     cudaStream_t s) {
+  switch (L.emu_per_16) {
+    case 0: return launch_inst<D, CAUSAL, VARLEN, 0>(L, tq, tk, tv, s);
+    case 2: return launch_inst<D, CAUSAL, VARLEN, 2>(L, tq, tk, tv, s);
+    case 3: return launch_inst<D, CAUSAL, VARLEN, 3>(L, tq, tk, tv, s);
+    case 4: return launch_inst<D, CAUSAL, VARLEN, 4>(L, tq, tk, tv, s);
+    default: return FA_ERR_INVALID_ARG;
+  }
+}
+
+template <int D>
+fa_status launch_d(const FwdLaunch& L, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   cudaStream_t s) {
+  const bool varlen = L.p.cu_seqlens != nullptr;
+  if (L.causal)
+    return varlen ? launch_emu<D, true, true>(L, tq, tk, tv, s) : launch_emu<D, true, false>(L, tq, tk, tv, s);
+  return varlen ? launch_emu<D, false, true>(L, tq, tk, tv, s) : launch_emu<D, false, false>(L, tq, tk, tv, s);
+}
+
+}  // namespace fwd
+
+fa_status launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  const int rows_q = L.p.cu_seqlens ? L.p.Sq : L.p.B * L.p.Sq;
+  const int rows_k = L.p.cu_seqlens ? L.p.Sk : L.p.B * L.p.Sk;
+  fa_status st;
+  if ((st = make_tmap_rows_heads_d(&tq, L.q, rows_q, L.p.Hq, L.D, fwd::kBM)) != FA_OK) return st;
+  if ((st = make_tmap_rows_heads_d(&tk, L.k, rows_k, L.p.Hkv, L.D, fwd::kBN)) != FA_OK) return st;
+  if ((st = make_tmap_rows_heads_d(&tv, L.v, rows_k, L.p.Hkv, L.D, fwd::kBN)) != FA_OK) return st;
+  if (L.D == 128) return fwd::launch_d<128>(L, tq, tk, tv, stream);
+  if (L.D == 64) return fwd::launch_d<64>(L, tq, tk, tv, stream);
+  return FA_ERR_UNSUPPORTED;
+}
+
+fa_status fwd_take_device_error() {
+  DeviceError e{0, 0};
+  if (cudaMemcpyFromSymbol(&e, fwd::g_err, sizeof(e)) != cudaSuccess) return FA_ERR_CUDA;
+  if (e.status != 0) {
+    const DeviceError z{0, 0};
+    if (cudaMemcpyToSymbol(fwd::g_err, &z, sizeof(z)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return static_cast<fa_status>(e.status);
+}
+
+}  // namespace fa

@@ -1,0 +1,96 @@
+// Host-side plumbing shared by the C ABI (fa_api.cu) and the kernel
+// translation units: launch descriptors, tensor-map construction and the
+// per-translation-unit device error records.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "fa.h"
+
+namespace fa {
+
+// Upper bounds of the packed-length scheduler tables kept in shared memory.
+constexpr int kMaxPackedSeqs = 1024;
+constexpr int kMaxPairsPerSeq = 1024;   // 256 query rows per pair -> 262,144 tokens
+
+struct FwdParams {
+  void* o;                 // BF16 output, same layout as q
+  float* lse;              // FP32 log-sum-exp
+  const int* cu_seqlens;   // device [B+1] or nullptr
+  int B, Hq, Hkv, Sq, Sk;  // packed: Sq = Sk = total tokens
+  int group;               // Hq / Hkv
+  float scale_log2;        // scale * log2(e)
+  float thr;               // lazy-rescale threshold in log2 units
+  unsigned long long wait_limit_ns;
+};
+
+struct FwdLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  FwdParams p;
+  int D;
+  bool causal;
+  int emu_per_16;
+  int num_sms;
+};
+
+struct BwdParams {
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;     // [B, Sq, Hq, D] fp32
+  float* delta;      // [B, Hq, Sq]
+  float* lse2;       // [B, Hq, Sq]   lse * log2(e)
+  int* tickets;      // [B, Hq, ceil(Sq/128)] or nullptr
+  int B, Hq, Hkv, Sq, Sk, D;
+  int group;
+  int causal;
+  int deterministic;
+  float scale;
+  float scale_log2;
+  unsigned long long wait_limit_ns;
+};
+
+struct BwdLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  BwdParams p;
+  int num_sms;
+};
+
+// Workspace carve-up of the backward pass (all offsets 256-byte aligned).
+struct BwdWorkspace {
+  size_t dq_acc, delta, lse2, tickets, total;
+};
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic);
+
+// 3-D tiled tensor map over a [rows, heads, D] BF16 array (D contiguous) with
+// a box of 64 x 1 x box_rows and 128-byte swizzle.
+fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_rows);
+
+// Kernel launchers (defined in their translation units).
+fa_status launch_fwd(const FwdLaunch& L, cudaStream_t stream);
+fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+fa_status launch_diag_exp2(const float* x, float* y_emu, float* y_hw, long long n, cudaStream_t stream);
+fa_status launch_diag_wait(unsigned long long limit_ns, cudaStream_t stream);
+
+// Each translation unit keeps its own device error record; these read and
+// clear it (returning FA_OK when clean).
+fa_status fwd_take_device_error();
+fa_status bwd_take_device_error();
+fa_status diag_take_device_error();
+
+// Shared-memory alignment slack added to every dynamic allocation.
+constexpr int kSmemAlignSlack = 1024;
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+}  // namespace fa

@@ -1,0 +1,136 @@
+/*
+ * fa.h -- C ABI of the exact-attention library for one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  Exact scaled-dot-product attention and its gradients:
+ *
+ *     O   = softmax(scale * Q K^T [+ causal mask]) V
+ *     LSE = per-row log-sum-exp of the masked, scaled scores (natural log)
+ *
+ * evaluated tile by tile with an online softmax so that the score matrix never
+ * reaches device memory, plus the backward pass producing dQ, dK and dV.
+ * Sources: "FlashAttention-4: matrix throughput bottlenecks" (lecompute.fr),
+ * section "Between the matrix products the kernel must produce weights" (the
+ * definition: scores, row softmax, second product with V); "FlashAttention-4:
+ * Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware Scaling"
+ * (fdeinterviews.com summary), opening paragraph (tiling, online softmax, no
+ * full matrix in memory), bullets "Lazy rescaling" and "Paired-CTA backward
+ * pass", and the paragraph on causal masks, variable lengths and the
+ * deterministic backward mode.
+ *
+ * Conventions shared by every call.
+ *   - Element types: Q, K, V, O, dO, dQ, dK, dV are BF16; LSE is FP32.
+ *   - Dense layout (cu_seqlens == NULL): Q, O, dO, dQ are [B, Sq, Hq, D];
+ *     K, V, dK, dV are [B, Sk, Hkv, D]; LSE is [B, Hq, Sq].  All contiguous,
+ *     D innermost.
+ *   - Packed variable-length layout (cu_seqlens != NULL): sequence b owns
+ *     tokens [cu_seqlens[b], cu_seqlens[b+1]) of Q, K, V, O shaped [total, H, D];
+ *     LSE is [Hq, total].  cu_seqlens is an int32 DEVICE array of B + 1
+ *     non-decreasing offsets with cu_seqlens[0] = 0; the same offsets apply
+ *     to queries and keys.  Sq and Sk must both equal the total token count
+ *     cu_seqlens[B] (the row count of the packed arrays; the host cannot read
+ *     it from device memory without a synchronisation).  At most 1024
+ *     sequences of at most 262,144 tokens each.  Offsets that break these
+ *     rules are detected on the device: nothing is computed and
+ *     fa_get_device_error() reports FA_ERR_INVALID_ARG.
+ *   - Grouped-query attention: query head h reads key/value head
+ *     h / (Hq / Hkv); Hq must be a multiple of Hkv.
+ *   - Causal mask, bottom-right aligned: query i sees key j iff
+ *     j <= i + (Sk - Sq).  A query row that sees no key gets O = 0 and
+ *     LSE = -inf.
+ *   - scale must be finite and > 0 (callers normally pass 1/sqrt(D)).
+ *   - Head dimension D must be 64 or 128.
+ *   - Every pointer is caller-owned device memory, 16-byte aligned.  The
+ *     library allocates no device memory in these calls; the backward pass
+ *     takes its scratch from the caller's workspace.
+ *   - Calls are asynchronous on `stream`; argument errors are reported
+ *     synchronously by the return value before anything is launched.  A
+ *     device-side wait that exceeded its time bound is reported later by
+ *     fa_get_device_error().  No C++ exception crosses this interface.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols of the shared library. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad scale ... */
+  FA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (D, device) */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_TIMEOUT = 4,      /* a device-side pipeline wait exceeded its bound */
+  FA_ERR_WORKSPACE = 5     /* workspace missing, misaligned or too small */
+} fa_status;
+
+/*
+ * Forward pass.  Writes O and LSE.
+ *   q, k, v      device, BF16, layouts above
+ *   o            device, BF16, same shape as q
+ *   lse          device, FP32, [B, Hq, Sq] dense or [Hq, total] packed
+ *   B, Hq, Hkv   batch (number of sequences when packed) and head counts
+ *   Sq, Sk, D    sequence lengths (total tokens when packed) and head dim
+ *   causal       0 or 1
+ *   scale        multiplier of Q K^T
+ *   cu_seqlens   device int32 [B + 1], or NULL for the dense layout
+ * Returns FA_OK once the work is enqueued on `stream`.
+ */
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Sq, int Sk, int D, int causal, float scale, const int* cu_seqlens, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd() needs for this problem (dense layout).
+ * The workspace holds the FP32 dQ accumulator [B, Sq, Hq, D], the per-row
+ * terms Delta_i = sum_d dO_id * O_id and LSE * log2(e) (FP32 [B, Hq, Sq] each)
+ * and, when `deterministic` is set, one int32 ticket per (b, h, 128-row query
+ * block).  Returns 0 for arguments fa_bwd() would reject.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic);
+
+/*
+ * Backward pass of fa_fwd() for the dense layout.  Given the forward inputs,
+ * its outputs O and LSE, and the upstream gradient dO, writes dQ, dK, dV
+ * (BF16; dK/dV of a key/value head sum over its query-head group).
+ *   deterministic  0: dQ partial sums are added with FP32 atomics (order may
+ *                  vary run to run); 1: they are added in a fixed order so
+ *                  repeated calls give bitwise-identical dQ.
+ *   workspace      device, 256-byte aligned, at least
+ *                  fa_bwd_workspace_size(...) bytes; contents on entry are
+ *                  ignored and clobbered.
+ * cu_seqlens must be NULL: the packed-length backward is not built yet and
+ * returns FA_ERR_UNSUPPORTED.
+ */
+FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk,
+                        int D, int causal, float scale, const int* cu_seqlens, int deterministic,
+                        void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the first device-side
+ * failure recorded by any kernel of this library on the current device since
+ * the last call (FA_OK if none).  A pipeline wait that exceeds its bound
+ * (about two seconds) makes every role of the affected thread block stop and
+ * exit cleanly, records FA_ERR_TIMEOUT here and leaves the outputs undefined;
+ * the CUDA context stays usable.
+ */
+FA_API fa_status fa_get_device_error(fa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+FA_API const char* fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

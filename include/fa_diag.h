@@ -1,0 +1,64 @@
+/*
+ * fa_diag.h -- tuning and self-check entry points of the exact-attention
+ * library (same shared library as fa.h).  They exist so that tests and the
+ * benchmark can exercise the method's individual claims on the GPU; a normal
+ * caller only needs fa.h.
+ */
+#ifndef FA_GB300_FA_DIAG_H
+#define FA_GB300_FA_DIAG_H
+
+#include "fa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Forward-pass knobs (fa_fwd uses the defaults).
+ *   rescale_threshold  Lazy rescaling: the running output of a row is
+ *                      rescaled only when the row maximum grows by more than
+ *                      this many log2 units; 8.0 is the method's value
+ *                      ("FlashAttention-4: Algorithm and Kernel Pipelining
+ *                      Co-Design ...", bullet "Lazy rescaling").  0.0 gives
+ *                      the classic eager online softmax.  Must be in [0, 16]:
+ *                      larger values let unnormalised weights overflow.
+ *   emu_per_16         How many of every 16 softmax exponentials are computed
+ *                      by the FMA-unit polynomial instead of the hardware
+ *                      exponential (same page, bullet "Software
+ *                      exponentials", which uses 10-25%): 0, 2, 3 or 4.
+ *                      Negative selects the library default.
+ */
+typedef struct {
+  float rescale_threshold;
+  int emu_per_16;
+} fa_fwd_tuning;
+
+/* The defaults fa_fwd() uses. */
+FA_API fa_fwd_tuning fa_fwd_default_tuning(void);
+
+/* fa_fwd() with explicit knobs; `t` may be NULL for the defaults. */
+FA_API fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                           int Hkv, int Sq, int Sk, int D, int causal, float scale, const int* cu_seqlens,
+                           const fa_fwd_tuning* t, fa_stream_t stream);
+
+/*
+ * Evaluates 2^x for n FP32 inputs both ways the softmax can: y_emu with the
+ * FMA-unit polynomial (split x into floor and fraction, cubic on the
+ * fraction, add the integer to the exponent bits), y_hw with the hardware
+ * exponential instruction.  All pointers are device memory.
+ */
+FA_API fa_status fa_diag_exp2(const float* x, float* y_emu, float* y_hw, long long n, fa_stream_t stream);
+
+/*
+ * Launches one thread block that waits on a pipeline barrier nothing will
+ * ever complete, with a time bound of `limit_ns`.  The wait gives up, the
+ * block exits cleanly, and the next fa_get_device_error() returns
+ * FA_ERR_TIMEOUT.  Used to test the bounded-wait path without hanging the GPU.
+ */
+FA_API fa_status fa_diag_wait_timeout(unsigned long long limit_ns, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_DIAG_H */
