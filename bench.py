@@ -1,0 +1,373 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic BF16
+input: the forward call (O, LSE) followed, once built, by the backward call
+(dQ, dK, dV) on the same tensors.  Default workload: dense B=4, H=16,
+S=4096, D=128 (non-causal; --causal for the masked variant).
+
+Prints ONE JSON line (rank 0).  `value` is whole-job TFLOPS
+(forward 4*B*Hq*Sq*Sk*D, halved when causal; backward 2.5x that) over all
+ranks, timed with CUDA events on the launching stream with inputs resident in
+HBM; `e2e` times the same steps through the public API from pinned host
+buffers, including host->device and device->host copies.
+
+--impl reference times the CPU oracle (fp64 numpy) on a bounded sample of the
+same workload instead: the pages ship no code to run, so the oracle is the
+reference arm.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from exact_attention_78_gb300 import flops as F  # noqa: E402
+from exact_attention_78_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOPS on 1 GB300, BF16 D=128 S=1K–32K; % of BF16 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true", help="time the forward call alone")
+    ap.add_argument("--B", type=int, default=4)
+    ap.add_argument("--H", type=int, default=16)
+    ap.add_argument("--S", type=int, default=4096)
+    ap.add_argument("--D", type=int, default=128)
+    ap.add_argument("--emu", type=int, default=None, help="exp2 emulation: entries of every 16 on FMA")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                     timeout=5).stdout.strip()
+                if out:
+                    self.samples.append([x.strip() for x in out.split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [v for v in (num(s[1]) for s in self.samples) if v is not None]
+        mx = [v for v in (num(s[2]) for s in self.samples) if v is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if len(s) > 4 + i and s[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def workload(args):
+    return W.Workload("dense_causal" if args.causal else "dense", B=args.B, Hq=args.H, Hkv=args.H, Sq=args.S,
+                      Sk=args.S, D=args.D, causal=args.causal)
+
+
+def step_flops(w, with_bwd):
+    f = F.fwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
+    return f + (F.bwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal) if with_bwd else 0.0)
+
+
+# --------------------------------------------------------------- oracle arm --
+
+def oracle_sample(w, seconds=15.0, with_bwd=True):
+    """Times the fp64 oracle on whole heads of the workload until about
+    `seconds` have passed (at least one head); returns (TFLOPS, description,
+    threads, seconds per head)."""
+    import oracle
+    one = W.Workload("s", B=1, Hq=1, Hkv=1, Sq=w.Sq, Sk=w.Sk, D=w.D, causal=w.causal)
+    (q, k, v, do), _ = W.make_inputs(one, with_grad=True)
+
+    def f64(t):
+        return t.float().numpy().astype(np.float64)[0, :, 0]
+
+    qh, kh, vh, doh = f64(q), f64(k), f64(v), f64(do)
+    per_head = F.fwd_flops(1, 1, w.Sq, w.Sk, w.D, w.causal)
+    if with_bwd:
+        per_head += F.bwd_flops(1, 1, w.Sq, w.Sk, w.D, w.causal)
+    t0 = time.perf_counter()
+    heads = 0
+    while True:
+        oracle.head_forward(qh, kh, vh, w.causal, w.scale)
+        if with_bwd:
+            oracle.head_backward(qh, kh, vh, doh, w.causal, w.scale)
+        heads += 1
+        if time.perf_counter() - t0 >= seconds or heads >= w.B * w.Hq:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        threads = len(os.sched_getaffinity(0))
+    except AttributeError:
+        threads = os.cpu_count()
+    desc = "%d of %d (b,h) heads, %s, S=%d D=%d, numpy fp64 (BLAS threads = affinity)" % (
+        heads, w.B * w.Hq, "fwd+bwd" if with_bwd else "fwd", w.Sq, w.D)
+    return heads * per_head / dt / 1e12, desc, threads, dt / heads
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = workload(args)
+    with_bwd = not args.fwd_only
+    for _ in range(args.warmup):
+        oracle_sample(w, seconds=0.0, with_bwd=with_bwd)
+    vals, per_head = [], []
+    desc = threads = None
+    for _ in range(args.steps):
+        v, desc, threads, sph = oracle_sample(w, seconds=0.0, with_bwd=with_bwd)
+        vals.append(v)
+        per_head.append(sph)
+    val = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(per_head) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {**w.describe(), "step": "fwd+bwd" if with_bwd else "fwd",
+                       "sample": "one (b,h) head of the workload per step"},
+            "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm --
+
+def run_gpu(args):
+    import exact_attention_78_gb300 as fa
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fa.load_library(build_if_missing=(rank == 0))
+    w = workload(args)
+    (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    have_bwd = not args.fwd_only
+    ws_buf = dq = dk = dv = None
+    if have_bwd:
+        try:
+            need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, False)
+            ws_buf = torch.empty(need, dtype=torch.uint8, device="cuda")
+            dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+            fa.fwd(qd, kd, vd, causal=w.causal, out=o, lse=lse, emu_per_16=args.emu)
+            fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, workspace=ws_buf, dq=dq, dk=dk, dv=dv)
+        except fa.FAError as e:
+            if e.status != 2:
+                raise
+            have_bwd = False
+    torch.cuda.synchronize()
+
+    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def step(i=None):
+        if i is not None:
+            ev_f0[i].record(stream)
+        fa.fwd(qd, kd, vd, causal=w.causal, out=o, lse=lse, emu_per_16=args.emu)
+        if i is not None:
+            ev_f1[i].record(stream)
+        if have_bwd:
+            fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, workspace=ws_buf, dq=dq, dk=dk, dv=dv)
+        if i is not None:
+            ev_b1[i].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = fa.get_device_error()
+    if st != 0:
+        raise RuntimeError("device error during warm-up: %s" % fa.status_string(st))
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    if fa.get_device_error() != 0:
+        raise RuntimeError("device error in timed region")
+    elapsed_ms = start.elapsed_time(end)
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t)
+    fwd_ms = statistics.mean(ev_f0[i].elapsed_time(ev_f1[i]) for i in range(args.steps))
+    bwd_ms = statistics.mean(ev_f1[i].elapsed_time(ev_b1[i]) for i in range(args.steps)) if have_bwd else 0.0
+
+    flops_step = step_flops(w, have_bwd)
+    ms_step = elapsed_ms / args.steps
+    value = ws * flops_step / (ms_step * 1e-3) / 1e12
+
+    # end to end: pinned host inputs -> device -> fwd(+bwd) -> host outputs
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        hg = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (qd, kd, vd)] if have_bwd else []
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hdo,) if have_bwd else ()))
+        d2h = ho.numel() * 2 + hl.numel() * 4 + sum(t.numel() * 2 for t in hg)
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            if have_bwd:
+                dod.copy_(hdo, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            if have_bwd:
+                for hgt, g in zip(hg, (dq, dk, dv)):
+                    hgt.copy_(g, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, args.steps // 4)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / n_e2e
+        if ws > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t)
+        e2e = {"value": ws * flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    pk, pk_kind = peaks()
+    # dominant kernel: the longer of the forward kernel and the backward call
+    if have_bwd and bwd_ms > fwd_ms:
+        dom, dom_ms, dom_flops = "bwd", bwd_ms, F.bwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
+    else:
+        dom, dom_ms, dom_flops = "fwd", fwd_ms, F.fwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "kernel": dom,
+                "peak_kind": "%s, sustained bf16 (kernel timed inside a repeated step)" % pk_kind}
+
+    cpu = None
+    if not args.no_cpu:
+        cpu_v, cpu_desc, cpu_threads, _ = oracle_sample(w, seconds=12.0, with_bwd=have_bwd)
+        cpu = {"value": cpu_v, "unit": "TFLOPS", "cores": cpu_threads, "kind": "oracle", "sample": cpu_desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**w.describe(), "step": "fwd+bwd" if have_bwd else "fwd",
+                   "l2": "inputs larger than L2 (Q,K,V,O %d MiB each)" % (qd.numel() * 2 >> 20),
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "fwd_tflops": F.fwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal) / (fwd_ms * 1e-3) / 1e12,
+        "fwd_ms": fwd_ms,
+        "bwd_tflops": (F.bwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal) / (bwd_ms * 1e-3) / 1e12
+                       if have_bwd else None),
+        "bwd_ms": bwd_ms if have_bwd else None,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (1 + (3 if have_bwd else 0)),
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

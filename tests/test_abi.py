@@ -1,0 +1,117 @@
+"""The C-ABI shared library on the host, without a GPU: it builds, loads,
+exports every function the public headers declare, and rejects bad
+arguments synchronously before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import exact_attention_78_gb300 as fa
+    return fa.load_library(build_if_missing=True)
+
+
+def _declared():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        with open(os.path.join(ROOT, "include", h)) as f:
+            text = f.read()
+        names += re.findall(r"^FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_device_error", "fa_status_string",
+            "fa_fwd_ex", "fa_diag_exp2", "fa_diag_wait_timeout"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA",
+                                 "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE"]):
+        assert lib.fa_status_string(code).decode() == name
+    assert lib.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+
+
+# Pointers that are never dereferenced: validation rejects every call below
+# before any CUDA call is made.
+A = ctypes.c_void_p(1 << 20)          # 16-byte aligned fake address
+MIS = ctypes.c_void_p((1 << 20) + 8)  # misaligned
+
+
+def _fwd(lib, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=2, Sq=128, Sk=128, D=128, causal=0, scale=0.125,
+         cu=None):
+    return lib.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, cu, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(o=MIS), 1), (dict(k=MIS), 1),
+    (dict(B=0), 1), (dict(Sq=0), 1), (dict(Sk=-3), 1), (dict(Hq=3, Hkv=2), 1),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(causal=2), 1), (dict(D=96), 2), (dict(D=256), 2),
+    (dict(cu=ctypes.c_void_p(A.value), Sq=100, Sk=120), 1),
+    (dict(cu=ctypes.c_void_p(A.value + 2)), 1),
+    (dict(cu=ctypes.c_void_p(A.value), B=2000), 2),
+])
+def test_forward_rejects_bad_arguments(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+
+
+def test_forward_tuning_validation(lib):
+    from exact_attention_78_gb300.binding import FwdTuning
+    t = lib.fa_fwd_default_tuning()
+    assert t.rescale_threshold == 8.0 and t.emu_per_16 in (0, 2, 3, 4)
+    for thr, emu in ((-1.0, 0), (17.0, 0), (8.0, 1), (8.0, 5), (float("nan"), 0)):
+        bad = FwdTuning(thr, emu)
+        assert lib.fa_fwd_ex(A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, 0.125, None, ctypes.byref(bad), None) == 1
+
+
+def test_workspace_size(lib):
+    n = lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 0)
+    acc = 2 * 8192 * 16 * 128 * 4
+    rows = 2 * 16 * 8192 * 4
+    assert n == acc + 2 * rows
+    det = lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 1)
+    assert det == n + 2 * 16 * 64 * 4
+    assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 96, 0) == 0
+    assert lib.fa_bwd_workspace_size(2, 15, 4, 8192, 8192, 128, 0) == 0
+    assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 3) == 0
+
+
+def test_backward_rejects_bad_arguments(lib):
+    def call(ws=A, ws_bytes=1 << 40, cu=None, det=0, D=128, dq=A):
+        return lib.fa_bwd(A, A, A, A, A, A, dq, A, A, 1, 2, 2, 128, 128, D, 0, 0.125, cu, det, ws, ws_bytes, None)
+    assert call(dq=None) == 1
+    assert call(dq=MIS) == 1
+    assert call(det=2) == 1
+    assert call(D=80) == 2
+    assert call(cu=A) == 2
+    assert call(ws=None) == 5
+    assert call(ws=ctypes.c_void_p(A.value + 16)) == 5
+    assert call(ws_bytes=100) == 5
+
+
+def test_diag_argument_checks(lib):
+    assert lib.fa_diag_exp2(None, None, None, -1, None) == 1
+    assert lib.fa_diag_exp2(None, None, None, 10, None) == 1
+    assert lib.fa_diag_exp2(None, None, None, 0, None) == 0
+    assert lib.fa_diag_wait_timeout(0, None) == 1
+    assert lib.fa_diag_wait_timeout(20_000_000_000, None) == 1
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    import exact_attention_78_gb300 as fa
+    x = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd(x, x, x)
