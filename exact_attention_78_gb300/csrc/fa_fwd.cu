@@ -306,15 +306,16 @@ __device__ void softmax_role(const int t, const Shared<D, VARLEN>& sh, const uin
         for (int c = 0; c < 128; ++c)
           if (c >= lim) r[c / 32][c % 32] = __float_as_uint(-INFINITY);
       }
-      // row maximum of the raw scores (scale > 0)
-      float mx[8];   // mx[i] covers columns [16 i, 16 i + 16)
+      // row maximum of the raw scores (scale > 0), with 3-input max
+      float mx[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(r[i / 2][(i % 2) * 16]);
+      for (int g = 0; g < 4; ++g) {
+        float m = __uint_as_float(r[g][0]);
 #pragma unroll
-      for (int c = 0; c < 128; ++c)
-        if ((c % 16) != 0) mx[c / 16] = fmaxf(mx[c / 16], __uint_as_float(r[c / 32][c % 32]));
-      const float m_blk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        for (int c = 1; c < 31; c += 2) m = max3(m, __uint_as_float(r[g][c]), __uint_as_float(r[g][c + 1]));
+        mx[g] = fmaxf(m, __uint_as_float(r[g][31]));
+      }
+      const float m_blk = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
       // lazy rescaling: move the running maximum only when it grows by more
       // than the threshold; otherwise keep the stale one (weights <= 2^thr)
       float factor = 1.0f;
@@ -330,21 +331,28 @@ __device__ void softmax_role(const int t, const Shared<D, VARLEN>& sh, const uin
       // Two row sums: of the FP32 weights (for the log-sum-exp) and of the
       // BF16-rounded weights the PV product actually multiplies V by (for the
       // final division, so the weights used sum to one; under a stale maximum
-      // the largest weight is not 1 and not exact in BF16).
-      float se[2] = {0.f, 0.f}, sr[2] = {0.f, 0.f};
+      // the largest weight is not 1 and not exact in BF16).  Pairs of columns
+      // go through packed FP32x2 instructions.
+      const uint64_t sl2x2 = pk2(sl2, sl2), negm2 = pk2(-m_use, -m_use);
+      uint64_t se2[4] = {0ull, 0ull, 0ull, 0ull}, sr2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        const float x0 = fmaf(__uint_as_float(r[c / 32][c % 32]), sl2, -m_use);
-        const float x1 = fmaf(__uint_as_float(r[(c + 1) / 32][(c + 1) % 32]), sl2, -m_use);
-        const float e0 = exp2_mixed<EMU>(x0, c), e1 = exp2_mixed<EMU>(x1, c + 1);
+        const uint64_t x2 = fma2(pk2(__uint_as_float(r[c / 32][c % 32]), __uint_as_float(r[c / 32][c % 32 + 1])),
+                                 sl2x2, negm2);
+        float x0, x1, e0, e1;
+        up2(x2, x0, x1);
+        exp2_pair<EMU>(x0, x1, c, e0, e1);
         const uint32_t pp = pack_bf16x2(e0, e1);
         pk[c / 64][(c / 2) % 32] = pp;
-        se[(c / 2) & 1] += e0 + e1;
-        sr[(c / 2) & 1] += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u);
+        se2[(c / 2) & 3] = add2(se2[(c / 2) & 3], pk2(e0, e1));
+        sr2[(c / 2) & 3] = add2(sr2[(c / 2) & 3], pk2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u)));
       }
-      l_run = l_run * factor + (se[0] + se[1]);
-      lr_run = lr_run * factor + (sr[0] + sr[1]);
+      float a0, a1, b0, b1;
+      up2(add2(add2(se2[0], se2[1]), add2(se2[2], se2[3])), a0, a1);
+      up2(add2(add2(sr2[0], sr2[1]), add2(sr2[2], sr2[3])), b0, b1);
+      l_run = l_run * factor + (a0 + a1);
+      lr_run = lr_run * factor + (b0 + b1);
       tmem_st32(tm_s + 0, pk[0]);      // P over the first 64 columns of S
       tmem_st32(tm_s + 32, pk[1]);
       tmem_st_wait();
@@ -391,8 +399,14 @@ __device__ void correction_role(const Shared<D, VARLEN>& sh, const uint32_t tmem
               tmem_ld32(tm_o + c * 32, r);
               tmem_ld_wait();
               tmem_ld_fence(r);
+              const uint64_t f2 = pk2(f, f);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+              for (int i = 0; i < 32; i += 2) {
+                float y0, y1;
+                up2(mul2(pk2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), f2), y0, y1);
+                r[i] = __float_as_uint(y0);
+                r[i + 1] = __float_as_uint(y1);
+              }
               tmem_st32(tm_o + c * 32, r);
             }
             tmem_st_wait();
