@@ -86,15 +86,16 @@ fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, i
 
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic) {
   BwdWorkspace w{};
+  const size_t sq_pad = (size_t(Sq) + 63) / 64 * 64;
   size_t off = 0;
   w.dq_acc = off;
   off = align256(off + (size_t)B * Sq * Hq * D * sizeof(float));
-  w.delta = off;
-  off = align256(off + (size_t)B * Hq * Sq * sizeof(float));
-  w.lse2 = off;
-  off = align256(off + (size_t)B * Hq * Sq * sizeof(float));
+  w.ndelta = off;
+  off = align256(off + (size_t)B * Hq * sq_pad * sizeof(float));
+  w.nlse2 = off;
+  off = align256(off + (size_t)B * Hq * sq_pad * sizeof(float));
   w.tickets = off;
-  if (deterministic) off = align256(off + (size_t)B * Hq * ((Sq + 127) / 128) * sizeof(int));
+  if (deterministic) off = align256(off + (size_t)B * Hq * (sq_pad / 64) * sizeof(int));
   w.total = off;
   return w;
 }
@@ -168,6 +169,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic) {
   if (check_shapes(B, Hq, Hkv, Sq, Sk, D, 1.0f, nullptr) != FA_OK) return 0;
   if (deterministic != 0 && deterministic != 1) return 0;
+  if (D != 128) return 0;
   return bwd_workspace_layout(B, Hq, Sq, D, deterministic).total;
 }
 
@@ -184,7 +186,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
     fa_status st = check_shapes(B, Hq, Hkv, Sq, Sk, D, scale, cu_seqlens);
     if (st != FA_OK) return st;
-    if (cu_seqlens != nullptr) return FA_ERR_UNSUPPORTED;
+    if (cu_seqlens != nullptr || D != 128) return FA_ERR_UNSUPPORTED;
     const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Sq, D, deterministic);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < ws.total)
       return FA_ERR_WORKSPACE;
@@ -202,8 +204,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     L.p.dk = dk;
     L.p.dv = dv;
     L.p.dq_acc = reinterpret_cast<float*>(wb + ws.dq_acc);
-    L.p.delta = reinterpret_cast<float*>(wb + ws.delta);
-    L.p.lse2 = reinterpret_cast<float*>(wb + ws.lse2);
+    L.p.ndelta = reinterpret_cast<float*>(wb + ws.ndelta);
+    L.p.nlse2 = reinterpret_cast<float*>(wb + ws.nlse2);
+    L.p.sq_pad = (Sq + 63) / 64 * 64;
+    L.p.nqb = L.p.sq_pad / 64;
     L.p.tickets = deterministic ? reinterpret_cast<int*>(wb + ws.tickets) : nullptr;
     L.p.B = B;
     L.p.Hq = Hq;

@@ -1,15 +1,646 @@
-// Backward pass (kernels not yet built: fa_bwd reports FA_ERR_UNSUPPORTED).
+// Backward pass of exact attention on sm_103a (dense layout, D = 128).
+//
+// Three kernels per call:
+//   pre   Delta_i = sum_d dO_id * O_id and LSE_i * log2(e) per query row (FP32,
+//         rows padded to a multiple of 64), the FP32 dQ accumulator and the
+//         deterministic-mode tickets zeroed;
+//   main  one persistent, warp-specialised CTA per SM; a work unit is one block
+//         of 128 keys of one (batch, key/value head).  For every query head of
+//         the group and every 64-row query block it recomputes the scores and
+//         runs the five products of the backward pass on the tensor cores
+//         (tcgen05, accumulators in TMEM):
+//             S^T  = K Q_i^T            dP^T = V dO_i^T
+//             P^T  = exp2(S^T * scale * log2 e - LSE2_i)
+//             dS^T = P^T * (dP^T - Delta_i)
+//             dV  += P^T dO_i           dK  += dS^T Q_i
+//             dQ_i^T = K^T dS^T   -> added to the FP32 accumulator
+//         dK and dV stay in TMEM across the whole group and are written once
+//         per unit, so they need no atomics.  dQ partial sums are added with
+//         FP32 reductions, or, in deterministic mode, in ascending key-block
+//         order enforced by one ticket per (batch, head, query block);
+//   post  dQ = BF16(scale * accumulator).
+//
+// Sources: "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
+// Asymmetric Hardware Scaling" (fdeinterviews.com summary): the paragraph on
+// Blackwell's changed balance (the backward tile: five products, shared-memory
+// traffic the bottleneck), bullet "Paired-CTA backward pass" (dQ through global
+// atomic adds) and the paragraph on the deterministic backward mode and
+// longest-first ordering.  The paired-CTA (2-SM) MMA of that bullet is not
+// used here yet: every product runs on one SM's tensor core.
+//
+// Thread layout (384 threads, 12 warps, one CTA per SM):
+//   warps 0-3   P / dS elementwise warpgroup (one thread per key row)
+//   warps 4-7   dQ warpgroup (accumulator adds) and dK/dV epilogue
+//   warp  8     TMA producer (one lane)
+//   warp  9     TMEM owner + MMA issuer (one lane)
+//   warps 10-11 idle
+//
+// Tensor memory (512 columns): S^T [0,64) (P^T as BF16 in [0,32)),
+// dP^T [64,128) (dS^T as BF16 in [64,96)), dV [128,256), dK [256,384),
+// dQ^T buffers [384,448) and [448,512).
 #include <cuda_runtime.h>
+
+#include <cmath>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "softmax_math.cuh"
 
 namespace fa {
 namespace bwd {
+
 __device__ DeviceError g_err;
+
+constexpr int kD = 128;        // head dimension of this kernel
+constexpr int kBN = 128;       // keys per work unit
+constexpr int kBM = 64;        // query rows per step
+constexpr int kThreads = 384;
+constexpr int kStages = 3;     // Q / dO ring depth
+
+enum Site { kSiteEsS = 1, kSiteEsQ, kSiteEsDs, kSiteDqFull, kSiteDqTicket, kSiteAcc, kSiteMmaKV, kSiteMmaQ,
+            kSiteMmaP, kSiteMmaDq, kSiteMmaAcc, kSiteProdKV, kSiteProdQ };
+
+struct Layout {
+  static constexpr int kKTile = kBN * kD * 2;        // 32 KB, 2 chunks of 128 rows x 128 B
+  static constexpr int kKChunk = kBN * 128;          // 16 KB
+  static constexpr int kQTile = kBM * kD * 2;        // 16 KB, 2 chunks of 64 rows x 128 B
+  static constexpr int kQChunk = kBM * 128;          // 8 KB
+  static constexpr int kStageBytes = 2 * kQTile + 2 * kBM * 4;   // Q, dO, lse2, delta
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kKTile;
+  static constexpr int kStage0 = kV + kKTile;                     // 1024-aligned
+  static constexpr int kStageStride = (kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kDs = kStage0 + kStages * kStageStride;    // dS^T smem, 2 buffers of 16 KB
+  static constexpr int kDsBytes = kBN * 128;
+  static constexpr int kBars = kDs + 2 * kDsBytes;
+  // kv_full, kv_empty, qd_full[3], qd_empty[3], s_full, p_ready,
+  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 6 + 2;
+  static constexpr int kMisc = kBars + kNumBars * 8;              // tmem slot, abort, check-in count
+  static constexpr int kTotal = kMisc + 64;
+  static constexpr int kDynamic = kTotal + kSmemAlignSlack;
+  static_assert(kDynamic <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
+
+// ------------------------------------------------------------- pre / post --
+
+// One warp per padded query row (b, h, q): stores -LSE * log2(e) and -Delta
+// (negated so the main kernel adds them with one packed FMA / ADD) and zeroes
+// the row's dQ accumulator.  Rows q >= Sq (padding) and rows that saw no key
+// (LSE = -inf) get -inf and 0, so their weights come out as exactly 0.
+__global__ void pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                           const float* __restrict__ lse, float* __restrict__ ndelta, float* __restrict__ nlse2,
+                           float* __restrict__ dq_acc, int* __restrict__ tickets, long long n_tickets, int B,
+                           int Hq, int Sq, int sq_pad) {
+  const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)B * Hq * sq_pad;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long r = warp_id; r < rows; r += nwarps) {
+    const int q = (int)(r % sq_pad);
+    const long long bh = r / sq_pad;
+    const int h = (int)(bh % Hq);
+    const int b = (int)(bh / Hq);
+    float dl = 0.0f, l2 = -INFINITY;
+    if (q < Sq) {
+      const size_t off = ((size_t(b) * Sq + q) * Hq + h) * kD + lane * 4;
+      const uint2 ov = *reinterpret_cast<const uint2*>(o + off);
+      const uint2 gv = *reinterpret_cast<const uint2*>(dout + off);
+      const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
+      float acc = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float2 a = __bfloat1622float2(op[e]), g = __bfloat1622float2(gp[e]);
+        acc = fmaf(a.x, g.x, acc);
+        acc = fmaf(a.y, g.y, acc);
+      }
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+      dl = -acc;
+      const float lv = lse[(size_t(b) * Hq + h) * Sq + q];
+      l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
+      *reinterpret_cast<float4*>(dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (lane == 0) {
+      ndelta[r] = dl;
+      nlse2[r] = l2;
+    }
+  }
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (long long t = tid; t < n_tickets; t += (long long)gridDim.x * blockDim.x) tickets[t] = 0;
 }
 
-fa_status launch_bwd(const BwdLaunch&, cudaStream_t) { return FA_ERR_UNSUPPORTED; }
+// dQ = BF16(scale * accumulator), eight elements per thread.
+__global__ void post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, long long n8,
+                            float scale) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+    const float4 c = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+    uint4 out;
+    out.x = pack_bf16x2(a.x * scale, a.y * scale);
+    out.y = pack_bf16x2(a.z * scale, a.w * scale);
+    out.z = pack_bf16x2(c.x * scale, c.y * scale);
+    out.w = pack_bf16x2(c.z * scale, c.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = out;
+  }
+}
+
+// ------------------------------------------------------------ main kernel --
+
+// One work unit: key block n (128 keys) of one (batch, key/value head); its
+// steps run over the query heads of the group and the 64-row query blocks
+// that see at least one of its keys.
+struct Unit {
+  int b, hk, n;
+  int i0;      // first query block
+  int nq;      // query blocks per head (nqb - i0)
+  int steps;   // group * nq
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p) {
+  Unit w;
+  const int BH = p.B * p.Hkv;
+  w.n = u / BH;            // key blocks near the start see the most query rows: longest first
+  const int bh = u % BH;
+  w.b = bh / p.Hkv;
+  w.hk = bh % p.Hkv;
+  const int nqb = (p.Sq + kBM - 1) / kBM;
+  int i0 = 0;
+  if (p.causal) {
+    // query row q sees key j iff j <= q + (Sk - Sq); block i reaches key 128 n
+    // iff 64 i + 63 + (Sk - Sq) >= 128 n
+    const int x = kBN * w.n - (p.Sk - p.Sq) - (kBM - 1);
+    i0 = x <= 0 ? 0 : (x + kBM - 1) / kBM;
+  }
+  w.i0 = i0;
+  w.nq = nqb > i0 ? nqb - i0 : 0;
+  w.steps = p.group * w.nq;
+  return w;
+}
+
+struct Shared {
+  using L = Layout;
+  uint8_t* base;
+  uint32_t sbase;
+  FA_DEV uint32_t bar(int i) const { return sbase + L::kBars + 8 * i; }
+  FA_DEV uint32_t kv_full() const { return bar(0); }
+  FA_DEV uint32_t kv_empty() const { return bar(1); }
+  FA_DEV uint32_t qd_full(int s) const { return bar(2 + s); }
+  FA_DEV uint32_t qd_empty(int s) const { return bar(2 + kStages + s); }
+  FA_DEV uint32_t s_full() const { return bar(2 + 2 * kStages); }
+  FA_DEV uint32_t p_ready() const { return bar(3 + 2 * kStages); }
+  FA_DEV uint32_t dq_full(int b) const { return bar(4 + 2 * kStages + b); }
+  FA_DEV uint32_t dq_empty(int b) const { return bar(6 + 2 * kStages + b); }
+  FA_DEV uint32_t ds_free(int b) const { return bar(8 + 2 * kStages + b); }
+  FA_DEV uint32_t acc_full() const { return bar(10 + 2 * kStages); }
+  FA_DEV uint32_t acc_empty() const { return bar(11 + 2 * kStages); }
+  FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
+  FA_DEV uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + L::kMisc); }
+  FA_DEV int* det_count() const { return reinterpret_cast<int*>(base + L::kMisc + 8); }
+  FA_DEV uint32_t stage(int s) const { return sbase + L::kStage0 + s * L::kStageStride; }
+  FA_DEV const float* stage_nlse2(int s) const {
+    return reinterpret_cast<const float*>(base + L::kStage0 + s * L::kStageStride + 2 * L::kQTile);
+  }
+  FA_DEV const float* stage_ndelta(int s) const { return stage_nlse2(s) + kBM; }
+  FA_DEV uint32_t ds(int b) const { return sbase + L::kDs + b * L::kDsBytes; }
+  FA_DEV uint8_t* ds_ptr(int b) const { return base + L::kDs + b * L::kDsBytes; }
+};
+
+// TMEM columns
+constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDK = 256, kColDQ = 384;
+
+__device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUtensorMap* tk,
+                              const CUtensorMap* tv, const CUtensorMap* tdo, const BwdParams& p,
+                              const int total_units) {
+  uint32_t sit = 0, ukv = 0;
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit(u, p);
+    if (w.steps == 0) continue;
+    if (!mbar_wait_bounded(sh.kv_empty(), (ukv & 1) ^ 1, sh.abort(), &g_err, kSiteProdKV, p.wait_limit_ns)) return;
+    mbar_arrive_expect_tx(sh.kv_full(), 2 * Layout::kKTile);
+    const int krow = w.b * p.Sk + kBN * w.n;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      tma_load_3d(sh.sbase + Layout::kK + c * Layout::kKChunk, tk, sh.kv_full(), c * 64, w.hk, krow);
+      tma_load_3d(sh.sbase + Layout::kV + c * Layout::kKChunk, tv, sh.kv_full(), c * 64, w.hk, krow);
+    }
+    for (int s = 0; s < w.steps; ++s, ++sit) {
+      const int h = w.hk * p.group + s / w.nq;
+      const int i = w.i0 + s % w.nq;
+      const int st = sit % kStages;
+      if (!mbar_wait_bounded(sh.qd_empty(st), ((sit / kStages) & 1) ^ 1, sh.abort(), &g_err, kSiteProdQ,
+                             p.wait_limit_ns))
+        return;
+      mbar_arrive_expect_tx(sh.qd_full(st), 2 * Layout::kQTile + 2 * kBM * 4);
+      const int qrow = w.b * p.Sq + kBM * i;
+      const uint32_t sb = sh.stage(st);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(sb + c * Layout::kQChunk, tq, sh.qd_full(st), c * 64, h, qrow);
+        tma_load_3d(sb + Layout::kQTile + c * Layout::kQChunk, tdo, sh.qd_full(st), c * 64, h, qrow);
+      }
+      const size_t roff = (size_t(w.b) * p.Hq + h) * p.sq_pad + size_t(kBM) * i;
+      bulk_load(sb + 2 * Layout::kQTile, p.nlse2 + roff, kBM * 4, sh.qd_full(st));
+      bulk_load(sb + 2 * Layout::kQTile + kBM * 4, p.ndelta + roff, kBM * 4, sh.qd_full(st));
+    }
+    ++ukv;
+  }
+}
+
+__device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
+  constexpr uint32_t kIdS = idesc_bf16_f32(kBN, kBM, false, false);   // S^T, dP^T: 128 keys x 64 queries
+  constexpr uint32_t kIdG = idesc_bf16_f32(kBN, kD, false, true);     // dV, dK: A in TMEM, B MN-major
+  constexpr uint32_t kIdQ = idesc_bf16_f32(kD, kBM, true, true);      // dQ^T: A = K^T, B = dS^T
+  const uint32_t kb = sh.sbase + Layout::kK, vb = sh.sbase + Layout::kV;
+  uint32_t sit = 0, ukv = 0;
+
+  auto wait = [&](uint32_t bar, uint32_t parity, int site) -> bool {
+    if (!mbar_wait_bounded(bar, parity, sh.abort(), &g_err, site, p.wait_limit_ns)) return false;
+    tc_fence_after();
+    return true;
+  };
+  // S^T = K Q_i^T and dP^T = V dO_i^T (K-major operands, K = D in steps of 16)
+  auto issue_sdp = [&](int st) {
+    const uint32_t qb = sh.stage(st), gb = qb + Layout::kQTile;
+    const uint64_t dk = sdesc_sw128(kb, 16, 1024), dv = sdesc_sw128(vb, 16, 1024);
+    const uint64_t dq = sdesc_sw128(qb, 16, 1024), dg = sdesc_sw128(gb, 16, 1024);
+#pragma unroll 1
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      const uint32_t oa = ((kk >> 2) * Layout::kKChunk + (kk & 3) * 32) >> 4;
+      const uint32_t ob = ((kk >> 2) * Layout::kQChunk + (kk & 3) * 32) >> 4;
+      mma_ss(tmem + kColS, dk + oa, dq + ob, kIdS, kk > 0 ? 1u : 0u);
+      mma_ss(tmem + kColDP, dv + oa, dg + ob, kIdS, kk > 0 ? 1u : 0u);
+    }
+  };
+
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit(u, p);
+    if (w.steps == 0) continue;
+    if (!wait(sh.kv_full(), ukv & 1, kSiteMmaKV)) return;
+    if (!wait(sh.qd_full(sit % kStages), (sit / kStages) & 1, kSiteMmaQ)) return;
+    issue_sdp(sit % kStages);
+    mma_commit(sh.s_full());
+    for (int s = 0; s < w.steps; ++s, ++sit) {
+      const int st = sit % kStages, buf = sit & 1;
+      if (!wait(sh.p_ready(), sit & 1, kSiteMmaP)) return;
+      if (s == 0 && ukv > 0 && !wait(sh.acc_empty(), (ukv - 1) & 1, kSiteMmaAcc)) return;
+      // dV += P^T dO_i, dK += dS^T Q_i: A from TMEM (8 columns per 16 queries),
+      // B MN-major (D contiguous, 64-wide chunks 8 KB apart, 16 queries = 2 KB)
+      const uint64_t dgo = sdesc_sw128(sh.stage(st) + Layout::kQTile, Layout::kQChunk, 1024);
+      const uint64_t dqq = sdesc_sw128(sh.stage(st), Layout::kQChunk, 1024);
+#pragma unroll 1
+      for (int kk = 0; kk < kBM / 16; ++kk) {
+        const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+        mma_ts(tmem + kColDV, tmem + kColS + kk * 8, dgo + uint64_t(kk * (2048 >> 4)), kIdG, acc);
+        mma_ts(tmem + kColDK, tmem + kColDP + kk * 8, dqq + uint64_t(kk * (2048 >> 4)), kIdG, acc);
+      }
+      mma_commit(sh.qd_empty(st));
+      // next step's scores go ahead of this step's dQ product
+      if (s + 1 < w.steps) {
+        const uint32_t nx = sit + 1;
+        if (!wait(sh.qd_full(nx % kStages), (nx / kStages) & 1, kSiteMmaQ)) return;
+        issue_sdp(nx % kStages);
+        mma_commit(sh.s_full());
+      }
+      // dQ_i^T = K^T dS^T: M = D (K MN-major, chunks 16 KB apart), N = 64
+      // queries (dS^T MN-major), K = 128 keys in steps of 16 (2 KB)
+      if (!wait(sh.dq_empty(buf), ((sit >> 1) & 1) ^ 1, kSiteMmaDq)) return;
+      const uint64_t da = sdesc_sw128(kb, Layout::kKChunk, 1024);
+      const uint64_t db = sdesc_sw128(sh.ds(buf), Layout::kDsBytes, 1024);
+#pragma unroll 1
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_ss(tmem + kColDQ + buf * kBM, da + uint64_t(kk * (2048 >> 4)), db + uint64_t(kk * (2048 >> 4)), kIdQ,
+               kk > 0 ? 1u : 0u);
+      mma_commit(sh.dq_full(buf));
+      mma_commit(sh.ds_free(buf));
+    }
+    mma_commit(sh.acc_full());
+    mma_commit(sh.kv_empty());
+    ++ukv;
+  }
+}
+
+// P / dS warpgroup: thread = key row kr of the unit's key block, 64 query
+// columns per step.
+__device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const BwdParams& p,
+                                 const int total_units) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int kr = (warp & 3) * 32 + lane;
+  const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
+  const float sl2 = p.scale_log2;
+  const uint64_t sl2x2 = pk2(sl2, sl2);
+  const int diag = p.Sk - p.Sq;
+  uint32_t sit = 0;
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit(u, p);
+    const int key = kBN * w.n + kr;
+    for (int s = 0; s < w.steps; ++s, ++sit) {
+      const int i = w.i0 + s % w.nq;
+      const int st = sit % kStages, buf = sit & 1;
+      if (!mbar_wait_bounded(sh.qd_full(st), (sit / kStages) & 1, sh.abort(), &g_err, kSiteEsQ, p.wait_limit_ns))
+        return;
+      if (!mbar_wait_bounded(sh.s_full(), sit & 1, sh.abort(), &g_err, kSiteEsS, p.wait_limit_ns)) return;
+      tc_fence_after();
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(tl + kColS, sr[0]);
+      tmem_ld32(tl + kColS + 32, sr[1]);
+      tmem_ld32(tl + kColDP, dr[0]);
+      tmem_ld32(tl + kColDP + 32, dr[1]);
+      tmem_ld_wait();
+      tmem_ld_fence(sr[0]);
+      tmem_ld_fence(sr[1]);
+      tmem_ld_fence(dr[0]);
+      tmem_ld_fence(dr[1]);
+      // columns c < cmin are masked: keys past Sk, or (causal) queries that
+      // come before this key
+      int cmin = 0;
+      if (key >= p.Sk) cmin = kBM;
+      else if (p.causal) cmin = min(kBM, max(0, key - diag - kBM * i));
+      const float2* nl = reinterpret_cast<const float2*>(sh.stage_nlse2(st));
+      const float2* nd = reinterpret_cast<const float2*>(sh.stage_ndelta(st));
+      uint32_t pp[32], dd[32];
+#pragma unroll
+      for (int c = 0; c < kBM; c += 2) {
+        const float2 l2 = nl[c / 2], d2 = nd[c / 2];
+        const uint64_t x = fma2(pk2(__uint_as_float(sr[c / 32][c % 32]), __uint_as_float(sr[c / 32][c % 32 + 1])),
+                                sl2x2, pk2(l2.x, l2.y));
+        float x0, x1;
+        up2(x, x0, x1);
+        float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1);
+        if (c < cmin) p0 = 0.0f;
+        if (c + 1 < cmin) p1 = 0.0f;
+        const uint64_t g = add2(pk2(__uint_as_float(dr[c / 32][c % 32]), __uint_as_float(dr[c / 32][c % 32 + 1])),
+                                pk2(d2.x, d2.y));
+        float s0, s1;
+        up2(mul2(pk2(p0, p1), g), s0, s1);
+        pp[c / 2] = pack_bf16x2(p0, p1);
+        dd[c / 2] = pack_bf16x2(s0, s1);
+      }
+      // P^T and dS^T as BF16 into TMEM (A operands of dV and dK)
+      tmem_st32(tl + kColS, pp);
+      tmem_st32(tl + kColDP, dd);
+      // dS^T into shared memory (B operand of dQ^T): row kr, 128-byte rows,
+      // 16-byte chunk j stored at chunk j ^ (kr mod 8)
+      if (!mbar_wait_bounded(sh.ds_free(buf), ((sit >> 1) & 1) ^ 1, sh.abort(), &g_err, kSiteEsDs,
+                             p.wait_limit_ns))
+        return;
+      uint8_t* row = sh.ds_ptr(buf) + kr * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(row + ((j ^ (kr & 7)) << 4)) =
+            make_uint4(dd[4 * j], dd[4 * j + 1], dd[4 * j + 2], dd[4 * j + 3]);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(sh.p_ready());
+    }
+  }
+}
+
+// dQ warpgroup: thread = feature d; adds the 64 query columns of dQ_i^T to
+// the FP32 accumulator, then writes dK (scaled) and dV at the end of a unit.
+__device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int wq = warp & 3;
+  const int d = wq * 32 + lane;           // dQ^T lane = feature; dK/dV lane = key row
+  const uint32_t tl = tmem + (uint32_t(wq * 32) << 16);
+  const int first = threadIdx.x == 128;   // first thread of this warpgroup
+  uint32_t sit = 0, ukv = 0;
+  int det_target = 0;                     // check-ins expected so far (deterministic mode)
+  __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk);
+  __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit(u, p);
+    for (int s = 0; s < w.steps; ++s, ++sit) {
+      const int h = w.hk * p.group + s / w.nq;
+      const int i = w.i0 + s % w.nq;
+      const int buf = sit & 1;
+      if (!mbar_wait_bounded(sh.dq_full(buf), (sit >> 1) & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns))
+        return;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(tl + kColDQ + buf * kBM, v[0]);
+      tmem_ld32(tl + kColDQ + buf * kBM + 32, v[1]);
+      tmem_ld_wait();
+      tmem_ld_fence(v[0]);
+      tmem_ld_fence(v[1]);
+      tc_fence_before();
+      mbar_arrive(sh.dq_empty(buf));
+      // Deterministic mode: key blocks add into this (b, h, i) in ascending
+      // order n = 0, 1, ...  Every thread waits (bounded) for the ticket to
+      // reach n, adds, fences and checks in on a shared counter; the first
+      // thread waits (bounded) for all 128 check-ins and advances the ticket.
+      int* ticket = nullptr;
+      bool ok = true;
+      if (p.deterministic) {
+        ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(ticket) != w.n) {
+          if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
+            if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
+            st_shared(sh.abort(), 1);
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      if (ok) {
+        const int q0 = kBM * i;
+        const int nvalid = min(kBM, p.Sq - q0);
+        float* base = p.dq_acc + ((size_t(w.b) * p.Sq + q0) * p.Hq + h) * kD + d;
+        const size_t rstride = size_t(p.Hq) * kD;
+#pragma unroll
+        for (int c = 0; c < kBM; ++c)
+          if (c < nvalid) atomicAdd(base + c * rstride, __uint_as_float(v[c / 32][c % 32]));
+      }
+      if (p.deterministic) {
+        if (!ok) return;
+        __threadfence();
+        atomicAdd(sh.det_count(), 1);
+        det_target += 128;
+        if (first) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_shared_volatile(smem_u32(sh.det_count())) < det_target) {
+            if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
+              if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
+              st_shared(sh.abort(), 1);
+              return;
+            }
+          }
+          __threadfence();
+          st_release_gpu(ticket, w.n + 1);
+        } else {
+          // hold until this step's ticket advanced, so no thread checks in
+          // for the next step before all have checked in for this one
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(ticket) == w.n) {
+            if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
+              if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
+              st_shared(sh.abort(), 1);
+              return;
+            }
+            __nanosleep(64);
+          }
+        }
+      }
+      if (!ok) return;
+    }
+    // epilogue of the unit: dV and scale * dK rows in BF16
+    const int key = kBN * w.n + d;
+    const bool valid = key < p.Sk;
+    const size_t roff = ((size_t(w.b) * p.Sk + key) * p.Hkv + w.hk) * kD;
+    if (w.steps > 0) {
+      if (!mbar_wait_bounded(sh.acc_full(), ukv & 1, sh.abort(), &g_err, kSiteAcc, p.wait_limit_ns)) return;
+      tc_fence_after();
+    }
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+      const float mul = which ? p.scale : 1.0f;
+      __nv_bfloat16* dst = (which ? dk : dv) + roff;
+#pragma unroll 1
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t r[32];
+        if (w.steps > 0) {
+          tmem_ld32(tl + (which ? kColDK : kColDV) + c * 32, r);
+          tmem_ld_wait();
+          tmem_ld_fence(r);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
+            o.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
+            o.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
+            o.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
+            reinterpret_cast<uint4*>(dst + c * 32)[e] = o;
+          }
+        }
+      }
+    }
+    if (w.steps > 0) {
+      tc_fence_before();
+      mbar_arrive(sh.acc_empty());
+      ++ukv;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x / 32;
+  Shared sh;
+  sh.base = smem;
+  sh.sbase = smem_u32(smem);
+  if (threadIdx.x == 0) {
+    mbar_init(sh.kv_full(), 1);
+    mbar_init(sh.kv_empty(), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(sh.qd_full(s), 1);
+      mbar_init(sh.qd_empty(s), 1);
+    }
+    mbar_init(sh.s_full(), 1);
+    mbar_init(sh.p_ready(), 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sh.dq_full(b), 1);
+      mbar_init(sh.dq_empty(b), 128);
+      mbar_init(sh.ds_free(b), 1);
+    }
+    mbar_init(sh.acc_full(), 1);
+    mbar_init(sh.acc_empty(), 128);
+    st_shared(sh.abort(), 0);
+    *sh.det_count() = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8 && (threadIdx.x % 32) == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 9) {
+    tmem_alloc(sh.tmem_slot(), 512);
+    tmem_relinquish();
+  }
+  const int total_units = ((p.Sk + kBN - 1) / kBN) * p.B * p.Hkv;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sh.tmem_slot();
+  if (warp < 4) {
+    elementwise_role(sh, tmem, p, total_units);
+  } else if (warp < 8) {
+    dq_role(sh, tmem, p, total_units);
+  } else if (warp == 8) {
+    if ((threadIdx.x % 32) == 0) producer_role(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
+  } else if (warp == 9) {
+    if ((threadIdx.x % 32) == 0) mma_role(sh, tmem, p, total_units);
+  }
+  if (ld_shared_volatile(sh.abort())) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace bwd
+
+fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
+  const BwdParams& p = L.p;
+  if (p.D != bwd::kD) return FA_ERR_UNSUPPORTED;
+  CUtensorMap tq, tk, tv, tdo;
+  fa_status st;
+  if ((st = make_tmap_rows_heads_d(&tq, L.q, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
+  if ((st = make_tmap_rows_heads_d(&tdo, p.dout, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
+  if ((st = make_tmap_rows_heads_d(&tk, L.k, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
+  if ((st = make_tmap_rows_heads_d(&tv, L.v, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
+
+  // pre: Delta, LSE2, zero accumulator and tickets
+  const long long rows = (long long)p.B * p.Hq * p.sq_pad;
+  const long long n_tickets = p.deterministic ? (long long)p.B * p.Hq * p.nqb : 0;
+  long long pre_blocks = (rows * 32 + 255) / 256;
+  if (pre_blocks > 16 * L.num_sms) pre_blocks = 16 * L.num_sms;
+  if (pre_blocks < 1) pre_blocks = 1;
+  bwd::pre_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
+      reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
+      p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.B, p.Hq, p.Sq, p.sq_pad);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(bwd::bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bwd::Layout::kDynamic) != cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_done = true;
+  }
+  const long long units = (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
+  const int grid = (int)(units < L.num_sms ? units : L.num_sms);
+  bwd::bwd_kernel<<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+
+  // post: dQ = BF16(scale * accumulator)
+  const long long n8 = (long long)p.B * p.Sq * p.Hq * p.D / 8;
+  long long post_blocks = (n8 + 255) / 256;
+  if (post_blocks > 16 * L.num_sms) post_blocks = 16 * L.num_sms;
+  bwd::post_kernel<<<(unsigned)post_blocks, 256, 0, stream>>>(p.dq_acc, reinterpret_cast<__nv_bfloat16*>(p.dq),
+                                                              n8, p.scale);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 fa_status bwd_take_device_error() {
   DeviceError e{0, 0};

@@ -46,10 +46,12 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* dq_acc;     // [B, Sq, Hq, D] fp32
-  float* delta;      // [B, Hq, Sq]
-  float* lse2;       // [B, Hq, Sq]   lse * log2(e)
-  int* tickets;      // [B, Hq, ceil(Sq/128)] or nullptr
+  float* ndelta;     // [B, Hq, sq_pad]  -sum_d dO * O
+  float* nlse2;      // [B, Hq, sq_pad]  -lse * log2(e)
+  int* tickets;      // [B, Hq, nqb] or nullptr
   int B, Hq, Hkv, Sq, Sk, D;
+  int sq_pad;        // Sq rounded up to a multiple of 64
+  int nqb;           // 64-row query blocks: sq_pad / 64
   int group;
   int causal;
   int deterministic;
@@ -68,7 +70,7 @@ struct BwdLaunch {
 
 // Workspace carve-up of the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {
-  size_t dq_acc, delta, lse2, tickets, total;
+  size_t dq_acc, ndelta, nlse2, tickets, total;
 };
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic);
 

@@ -92,9 +92,10 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
 /*
  * Bytes of device workspace fa_bwd() needs for this problem (dense layout).
  * The workspace holds the FP32 dQ accumulator [B, Sq, Hq, D], the per-row
- * terms Delta_i = sum_d dO_id * O_id and LSE * log2(e) (FP32 [B, Hq, Sq] each)
- * and, when `deterministic` is set, one int32 ticket per (b, h, 128-row query
- * block).  Returns 0 for arguments fa_bwd() would reject.
+ * terms -Delta_i = -sum_d dO_id * O_id and -LSE * log2(e) (FP32
+ * [B, Hq, Sq rounded up to a multiple of 64] each) and, when `deterministic`
+ * is set, one int32 ticket per (b, h, 64-row query block).  Returns 0 for
+ * arguments fa_bwd() would reject (including D != 128).
  */
 FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic);
 
@@ -108,8 +109,9 @@ FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int 
  *   workspace      device, 256-byte aligned, at least
  *                  fa_bwd_workspace_size(...) bytes; contents on entry are
  *                  ignored and clobbered.
- * cu_seqlens must be NULL: the packed-length backward is not built yet and
- * returns FA_ERR_UNSUPPORTED.
+ * Not built yet, and rejected with FA_ERR_UNSUPPORTED: the packed-length
+ * layout (cu_seqlens != NULL) and head dimensions other than 128.
+ * Launches three kernels on `stream` (row terms, main pass, dQ conversion).
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                         const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk,

@@ -82,8 +82,12 @@ def test_workspace_size(lib):
     rows = 2 * 16 * 8192 * 4
     assert n == acc + 2 * rows
     det = lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 1)
-    assert det == n + 2 * 16 * 64 * 4
+    assert det == n + 2 * 16 * 128 * 4          # one ticket per 64-row query block
+    # ragged rows: the per-row terms are padded to a multiple of 64 rows
+    r = lib.fa_bwd_workspace_size(1, 2, 2, 100, 100, 128, 0)
+    assert r == (1 * 100 * 2 * 128 * 4 + 255) // 256 * 256 + 2 * (1 * 2 * 128 * 4)
     assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 96, 0) == 0
+    assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 64, 0) == 0
     assert lib.fa_bwd_workspace_size(2, 15, 4, 8192, 8192, 128, 0) == 0
     assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 3) == 0
 
@@ -95,6 +99,7 @@ def test_backward_rejects_bad_arguments(lib):
     assert call(dq=MIS) == 1
     assert call(det=2) == 1
     assert call(D=80) == 2
+    assert call(D=64) == 2
     assert call(cu=A) == 2
     assert call(ws=None) == 5
     assert call(ws=ctypes.c_void_p(A.value + 16)) == 5

@@ -1,0 +1,121 @@
+"""Backward-pass parity on the GPU: dQ, dK, dV from the CUDA library (through
+its C ABI) against the fp64 oracle's analytic gradients on the same seeded
+BF16 inputs.  Relative Frobenius error <= 1e-2 per gradient.
+
+The GPU backward uses the GPU forward's BF16 O and FP32 LSE (as a training
+step would); the oracle uses its own fp64 O.  The difference is at the level
+of BF16 rounding and is covered by the tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_78_gb300 import workloads as W
+
+from parity import GRAD_RTOL, f64, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_78_gb300 as fa_mod
+    fa_mod.load_library(build_if_missing=True)
+    return fa_mod
+
+
+def _inputs(B, Hq, Hkv, Sq, Sk, seed=0, q_scale=1.0):
+    w = W.Workload("case", B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, D=128, causal=False, seed=seed, q_scale=q_scale)
+    (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
+    return q, k, v, do
+
+
+def _gpu_grads(fa, q, k, v, do, causal, deterministic=False):
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal=causal)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, deterministic=deterministic)
+    assert fa.get_device_error() == 0
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def _check(grads, q, k, v, do, causal):
+    ref = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), causal, 128 ** -0.5)
+    errs = []
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        gg = f64(g)
+        assert np.all(np.isfinite(gg)), name
+        e = rel_fro(gg, r)
+        errs.append(e)
+        assert e <= GRAD_RTOL, (name, e)
+    return errs
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_tile(fa, causal):
+    q, k, v, do = _inputs(1, 2, 2, 128, 128)
+    _check(_gpu_grads(fa, q, k, v, do, causal), q, k, v, do, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk", [
+    (1, 2, 2, 256, 256),
+    (2, 4, 2, 300, 300),     # grouped heads, ragged rows and keys
+    (1, 2, 1, 1000, 1000),   # several key blocks and query blocks
+    (1, 2, 2, 129, 257),     # Sq < Sk
+    (1, 2, 2, 520, 300),     # Sq > Sk: causal leaves the first rows without keys
+    (1, 1, 1, 1, 1),
+])
+def test_small_shapes_full_compare(fa, causal, B, Hq, Hkv, Sq, Sk):
+    q, k, v, do = _inputs(B, Hq, Hkv, Sq, Sk, seed=4)
+    _check(_gpu_grads(fa, q, k, v, do, causal), q, k, v, do, causal)
+
+
+def test_zero_queries_give_averaged_dv(fa):
+    """Closed form: Q = 0 -> uniform weights over the visible keys, so
+    dV_j = sum over rows i that see j of dO_i / (i + 1) (causal)."""
+    q, k, v, do = _inputs(1, 1, 1, 384, 384, seed=6)
+    q = torch.zeros_like(q)
+    _, _, dv = _gpu_grads(fa, q, k, v, do, True)
+    g = f64(do)[0, :, 0]
+    w = 1.0 / np.arange(1, 385)
+    ref = np.cumsum((g * w[:, None])[::-1], axis=0)[::-1]
+    assert rel_fro(f64(dv)[0, :, 0], ref) <= GRAD_RTOL
+
+
+def test_stress_logits(fa):
+    q, k, v, do = _inputs(1, 2, 2, 512, 512, seed=1, q_scale=4.0)
+    _check(_gpu_grads(fa, q, k, v, do, True), q, k, v, do, True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_deterministic_is_bitwise_repeatable(fa, causal):
+    q, k, v, do = _inputs(2, 4, 2, 700, 700, seed=8)
+    a = _gpu_grads(fa, q, k, v, do, causal, deterministic=True)
+    b = _gpu_grads(fa, q, k, v, do, causal, deterministic=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    _check(a, q, k, v, do, causal)
+    c = _gpu_grads(fa, q, k, v, do, causal, deterministic=False)
+    for x, y in zip(a, c):
+        assert rel_fro(f64(x), f64(y)) <= 2e-3
+
+
+# ---------------------------------------------------------------- full size --
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_training_shape_sampled_heads(fa, deterministic):
+    """B=2, H=16, S=8192, D=128, causal: gradients of whole heads compared."""
+    w = W.train(deterministic)
+    (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
+    dq, dk, dv = _gpu_grads(fa, q, k, v, do, True, deterministic=deterministic)
+    for t in (dq, dk, dv):
+        assert bool(torch.isfinite(t.float()).all())
+    heads = [(0, 0)] if deterministic else [(0, 3), (1, 15)]
+    for b, h in heads:
+        gq, gk, gv = oracle.head_backward(f64(q[b, :, h]), f64(k[b, :, h]), f64(v[b, :, h]), f64(do[b, :, h]),
+                                          True, w.scale)
+        for name, g, r in (("dq", dq[b, :, h], gq), ("dk", dk[b, :, h], gk), ("dv", dv[b, :, h], gv)):
+            e = rel_fro(f64(g), r)
+            assert e <= GRAD_RTOL, (b, h, name, e)
