@@ -46,6 +46,11 @@ def _check(grads, q, k, v, do, causal):
     for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
         gg = f64(g)
         assert np.all(np.isfinite(gg)), name
+        if np.linalg.norm(r) < 1e-9:
+            # an identically zero gradient (e.g. a single key: dS = 0, so dQ =
+            # dK = 0): only rounding noise may remain
+            assert np.max(np.abs(gg)) <= 1e-3, name
+            continue
         e = rel_fro(gg, r)
         errs.append(e)
         assert e <= GRAD_RTOL, (name, e)
