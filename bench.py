@@ -123,6 +123,30 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+def measured_traffic(kernel, w):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, if it
+    was taken on this workload and the kernel sources are unchanged since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    csrc = os.path.join(ROOT, "exact_attention_78_gb300", "csrc")
+    files = {"bwd_kernel": ["fa_bwd.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"],
+             "fwd_kernel": ["fa_fwd.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"]}[kernel]
+    m = hashlib.sha256()
+    for fn in files:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            m.update(f.read())
+    want = "dense B=%d Hq=Hkv=%d S=%d D=%d %s" % (w.B, w.Hq, w.Sq, w.D, "causal" if w.causal else "non-causal")
+    if m.hexdigest()[:16] != rec["source_sha"] or rec["workload"] != want:
+        return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+
+
 def workload(args):
     return W.Workload("dense_causal" if args.causal else "dense", B=args.B, Hq=args.H, Hkv=args.H, Sq=args.S,
                       Sk=args.S, D=args.D, causal=args.causal)
@@ -331,7 +355,7 @@ def run_gpu(args):
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "kernel": dom,
+                "frac": achieved / peak, "traffic": measured_traffic(dom + "_kernel", w), "kernel": dom,
                 "peak_kind": "%s, sustained bf16 (kernel timed inside a repeated step)" % pk_kind}
 
     cpu = None
