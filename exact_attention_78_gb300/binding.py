@@ -38,6 +38,8 @@ _SIGNATURES = {
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _i,
                     _vp, _sz, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
+                            _i, _vp]),
     "fa_get_device_error": (_i, [_vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_diag_exp2": (_i, [_vp, _vp, _vp, ctypes.c_longlong, _vp]),

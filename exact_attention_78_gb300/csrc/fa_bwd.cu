@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -652,4 +653,51 @@ fa_status bwd_take_device_error() {
   return static_cast<fa_status>(e.status);
 }
 
+// ------------------------------------------------- allocation-free entry --
+
+// Scratch of fa_bwd_noalloc(): a fixed buffer in the library's own device
+// memory, so that callers who may not allocate still get a backward pass.
+namespace bwd {
+static __device__ __align__(256) unsigned char g_static_scratch[FA_BWD_STATIC_SCRATCH_BYTES];
+}
+
+// Device address of the buffer on the current device, looked up once per
+// device (the symbol's host-side name is not a device address).
+static fa_status static_scratch_address(void** out) {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, bwd::g_static_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return FA_OK;
+}
+
 }  // namespace fa
+
+extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                    const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                                    int Sq, int Sk, int D, int causal, float scale, const int* cu_seqlens,
+                                    int deterministic, fa_stream_t stream) {
+  try {
+    const size_t need = fa_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic);
+    if (need > FA_BWD_STATIC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (need > 0) {  // need == 0: fa_bwd rejects the arguments below, before any launch
+      const fa_status st = fa::static_scratch_address(&scratch);
+      if (st != FA_OK) return st;
+    }
+    // fa_bwd's pre-pass zeroes the accumulator and tickets on every call, so
+    // what an earlier call left in the buffer does not matter.
+    return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, causal, scale, cu_seqlens,
+                  deterministic, scratch, scratch ? FA_BWD_STATIC_SCRATCH_BYTES : 0, stream);
+  } catch (...) {
+    return FA_ERR_CUDA;
+  }
+}

@@ -119,6 +119,32 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
                         void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * fa_bwd() for callers that cannot allocate device memory: some programs run
+ * under an allocator or serving runtime that owns every byte of the GPU and
+ * forbids allocating after start-up, or call from a point where an
+ * allocation would stall the device.  Arguments are those of fa_bwd() minus
+ * the workspace: the scratch comes from one buffer of
+ * FA_BWD_STATIC_SCRATCH_BYTES (64 MiB) compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  The paper has
+ * no counterpart; this is an interface convenience.
+ *   - Needs no more than fa_bwd_workspace_size(...) <= 64 MiB (for example
+ *     B * Sq * Hq * D * 4 bytes of dQ accumulator); larger problems are
+ *     rejected with FA_ERR_WORKSPACE before anything is launched.
+ *   - Allocates nothing.  The first call on a device looks up the buffer's
+ *     device address (cudaGetSymbolAddress) with that device current; make
+ *     that first call before any stream capture.
+ *   - All calls share the one buffer and it keeps the last call's contents;
+ *     the call clears what must start at zero itself.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on the
+ *     buffer: serialise them.
+ */
+#define FA_BWD_STATIC_SCRATCH_BYTES (64ull << 20)
+FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+                                int Sk, int D, int causal, float scale, const int* cu_seqlens, int deterministic,
+                                fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the first device-side
  * failure recorded by any kernel of this library on the current device since
  * the last call (FA_OK if none).  A pipeline wait that exceeds its bound
