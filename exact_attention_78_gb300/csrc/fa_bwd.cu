@@ -162,9 +162,14 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p) {
   Unit w;
-  const int BH = p.B * p.Hkv;
-  w.n = u / BH;            // key blocks near the start see the most query rows: longest first
-  const int bh = u % BH;
+  // Head-major: the key blocks of one (batch, kv head) are adjacent, so the
+  // CTAs working at the same time share that head's Q / dO reads and its
+  // slice of the dQ accumulator in L2.  Within a head, key blocks come in
+  // ascending order: under a causal mask the early blocks see the most query
+  // rows, so each head's longest units come first.
+  const int nkv = (p.Sk + kBN - 1) / kBN;
+  const int bh = u / nkv;
+  w.n = u % nkv;
   w.b = bh / p.Hkv;
   w.hk = bh % p.Hkv;
   const int nqb = (p.Sq + kBM - 1) / kBM;

@@ -29,7 +29,7 @@
 //   warps 4-7   softmax of query tile 1    (192)
 //   warps 8-11  correction + epilogue      (80)
 //   warp  12    TMA producer (one lane)    (48)
-//   warp  13    TMEM owner + MMA issuer    (48)
+//   warp  13    TMEM owner + MMA issuer    (48; converged warp, one elected lane issues)
 //   warps 14-15 idle                       (48)
 // Register budget: 2*128*192 + 128*80 + 128*48 = 65,536 = 512 threads x 128.
 //
@@ -470,7 +470,27 @@ __device__ void correction_role(const Shared<D, VARLEN>& sh, const uint32_t tmem
   }
 }
 
-// MMA issuer (one thread).  Issue order per unit, with tiles a = 0, b = 1:
+// Unrolled K steps of S = Q K^T (both operands K-major, 128-byte swizzle): step
+// kk reads 64-element chunk kk/4 at byte offset 32*(kk%4) inside its rows.
+template <int D, int CHUNK, int KK>
+FA_DEV void s_steps(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi, uint32_t idesc) {
+  if constexpr (KK < D / 16) {
+    constexpr uint32_t off = ((KK >> 2) * CHUNK + (KK & 3) * 32) >> 4;
+    mma_ss_w<off, off>(d_tmem, alo, ahi, blo, bhi, idesc, KK > 0 ? 1u : 0u);
+    s_steps<D, CHUNK, KK + 1>(d_tmem, alo, ahi, blo, bhi, idesc);
+  }
+}
+// Unrolled K steps of O += P V: step kk takes TMEM columns 8*kk.. of P and
+// key rows 16*kk.. of V (2048 bytes = 128 descriptor units further).
+template <int KK>
+FA_DEV void pv_steps(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi, uint32_t idesc, uint32_t acc) {
+  if constexpr (KK < kBN / 16) {
+    mma_ts_w<KK * 8, KK * 128>(d_tmem, a_tmem, blo, bhi, idesc, KK > 0 ? 1u : acc);
+    pv_steps<KK + 1>(d_tmem, a_tmem, blo, bhi, idesc, acc);
+  }
+}
+
+// MMA issuer (one converged warp; an elected lane issues).  Issue order per unit, with tiles a = 0, b = 1:
 //   S_a(0) S_b(0) | PV_a(0) S_a(1) PV_b(0) S_b(1) | PV_a(1) S_a(2) ... PV_b(n-1)
 // so that while the softmax of one tile runs, the tensor cores compute the
 // other tile's products.  S_t(j+1) overwrites the TMEM columns holding P_t(j)
@@ -485,29 +505,20 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
   const uint32_t kv_base = sh.sbase + L::kKV;
   uint32_t kv_it = 0, sit = 0, uit = 0;
 
-  // S_t = Q_t K^T : M = 128 rows, N = 128 keys, K = D in steps of 16
+  // S_t = Q_t K^T : M = 128 rows, N = 128 keys, K = D in steps of 16.  The
+  // descriptors of the 16-wide K steps differ from the first only in the
+  // start-address field, by compile-time offsets.
   auto issue_s = [&](int t, int stage) {
-    // descriptors differ only in the start-address field: step them
     const uint64_t da = sdesc_sw128(q_base + t * L::kTileBytes, 16, 1024);
     const uint64_t db = sdesc_sw128(kv_base + stage * L::kTileBytes, 16, 1024);
-    const uint32_t d_tmem = tmem + t * kBN;
-#pragma unroll 1
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
-      mma_ss(d_tmem, da + off, db + off, kIdS, kk > 0 ? 1u : 0u);
-    }
+    s_steps<D, L::kChunkBytes, 0>(tmem + t * kBN, desc_lo(da), desc_hi(da), desc_lo(db), desc_hi(db), kIdS);
   };
   // O_t (+)= P_t V : M = 128 rows, N = D, K = 128 keys in steps of 16;
-  // P from TMEM (8 columns per 16 keys), V MN-major (64-wide D chunks)
+  // P from TMEM (8 columns per 16 keys), V MN-major (64-wide D chunks;
+  // 16 keys = 16 rows of 128 B = 2048 B further into the V tile)
   auto issue_pv = [&](int t, int stage, bool acc) {
     const uint64_t db = sdesc_sw128(kv_base + stage * L::kTileBytes, L::kChunkBytes, 1024);
-    const uint32_t d_tmem = tmem + 256 + t * D;
-    const uint32_t a_tmem = tmem + t * kBN;
-#pragma unroll 1
-    for (int kk = 0; kk < kBN / 16; ++kk) {
-      // 16 keys = 16 rows of 128 B = 2048 B further into the V tile
-      mma_ts(d_tmem, a_tmem + kk * 8, db + uint64_t(kk * (2048 >> 4)), kIdPV, (acc || kk > 0) ? 1u : 0u);
-    }
+    pv_steps<0>(tmem + 256 + t * D, tmem + t * kBN, desc_lo(db), desc_hi(db), kIdPV, acc ? 1u : 0u);
   };
   auto wait_kv = [&](uint32_t it) -> bool {
     const int stage = it % L::kStages;
@@ -527,11 +538,11 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
     uint32_t k_it = kv_it++;
     if (!wait_kv(k_it)) return;
     issue_s(0, k_it % L::kStages);
-    mma_commit(sh.s_full(0));
+    mma_commit_w(sh.s_full(0));
     issue_s(1, k_it % L::kStages);
-    mma_commit(sh.s_full(1));
-    mma_commit(sh.kv_empty(k_it % L::kStages));
-    if (w.n == 1) mma_commit(sh.q_empty());
+    mma_commit_w(sh.s_full(1));
+    mma_commit_w(sh.kv_empty(k_it % L::kStages));
+    if (w.n == 1) mma_commit_w(sh.q_empty());
     for (int j = 0; j < w.n; ++j, ++sit) {
       const uint32_t v_it = kv_it++;
       if (!wait_kv(v_it)) return;
@@ -544,22 +555,22 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
       if (more) {
         if (!wait_kv(k_it)) return;
         issue_s(0, k_it % L::kStages);
-        mma_commit(sh.s_full(0));
+        mma_commit_w(sh.s_full(0));
       } else {
-        mma_commit(sh.o_full(0));
+        mma_commit_w(sh.o_full(0));
       }
       // tile 1: PV(j), then S(j+1)
       if (!mbar_wait_bounded(sh.o_ready(1), sit & 1, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return;
       tc_fence_after();
       issue_pv(1, v_it % L::kStages, j > 0);
-      mma_commit(sh.kv_empty(v_it % L::kStages));
+      mma_commit_w(sh.kv_empty(v_it % L::kStages));
       if (more) {
         issue_s(1, k_it % L::kStages);
-        mma_commit(sh.s_full(1));
-        mma_commit(sh.kv_empty(k_it % L::kStages));
-        if (j + 1 == w.n - 1) mma_commit(sh.q_empty());
+        mma_commit_w(sh.s_full(1));
+        mma_commit_w(sh.kv_empty(k_it % L::kStages));
+        if (j + 1 == w.n - 1) mma_commit_w(sh.q_empty());
       } else {
-        mma_commit(sh.o_full(1));
+        mma_commit_w(sh.o_full(1));
       }
     }
     ++uit;
@@ -665,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x % 32;
     if (warp == 12 && lane == 0)
       producer_role<D, CAUSAL, VARLEN>(sh, &tm_q, &tm_k, &tm_v, p, ps, total_units);
-    else if (warp == 13 && lane == 0)
+    else if (warp == 13)   // the whole warp, converged; one elected lane issues
       mma_role<D, CAUSAL, VARLEN>(sh, tmem, p, ps, total_units);
   }
 

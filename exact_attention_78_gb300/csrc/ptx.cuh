@@ -87,7 +87,7 @@ FA_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort, Dev
     if ((it & 15u) == 0u) {
       if (ld_shared_volatile(abort)) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
-        if (atomicCAS(&err->status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&err->site, site);
+        if (err && atomicCAS(&err->status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&err->site, site);
         st_shared(abort, 1);
         return false;
       }
@@ -198,6 +198,51 @@ FA_DEV void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t i
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+
+// Warp-collective forms: every lane of the warp executes the call with the
+// same operands; elect.sync picks one lane to issue.  Descriptors are passed
+// as (low word, high word) and the compile-time offsets AOFF / BOFF (in the
+// 16-byte units of the start-address field, or TMEM columns for a TMEM A
+// operand) are added inside the asm, so an unrolled sequence of K steps keeps
+// one base per operand live instead of one 64-bit descriptor per step.
+template <uint32_t AOFF, uint32_t BOFF>
+FA_DEV void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "add.u32 al, %1, %7;\n\t"
+      "add.u32 bl, %3, %8;\n\t"
+      "mov.b64 ad, {al, %2};\n\t"
+      "mov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+      : "memory");
+}
+template <uint32_t AOFF, uint32_t BOFF>
+FA_DEV void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b32 at, bl;\n\t.reg .b64 bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 at, %1, %6;\n\t"
+      "add.u32 bl, %2, %7;\n\t"
+      "mov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+      : "memory");
+}
+FA_DEV void mma_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(bar)
+      : "memory");
+}
+FA_DEV uint32_t desc_lo(uint64_t d) { return static_cast<uint32_t>(d); }
+FA_DEV uint32_t desc_hi(uint64_t d) { return static_cast<uint32_t>(d >> 32); }
 
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
