@@ -32,7 +32,7 @@
 //   warps 0-3   P / dS elementwise warpgroup (one thread per key row)
 //   warps 4-7   dQ warpgroup (accumulator adds) and dK/dV epilogue
 //   warp  8     TMA producer (one lane)
-//   warp  9     TMEM owner + MMA issuer (one lane)
+//   warp  9     TMEM owner + MMA issuer (converged warp, one elected lane issues)
 //   warps 10-11 idle
 //
 // Tensor memory (512 columns): S^T [0,64) (P^T as BF16 in [0,32)),
@@ -255,11 +255,48 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
   }
 }
 
+// Unrolled K steps (K = D in 16-wide steps) of S^T = K Q^T and dP^T = V dO^T;
+// all operands K-major: step kk reads 64-wide chunk kk/4 at byte 32*(kk%4).
+template <int KK>
+FA_DEV void sdp_steps(uint32_t d_s, uint32_t d_dp, uint32_t klo, uint32_t khi, uint32_t vlo, uint32_t vhi,
+                      uint32_t qlo, uint32_t qhi, uint32_t glo, uint32_t ghi, uint32_t idesc) {
+  if constexpr (KK < kD / 16) {
+    constexpr uint32_t oa = ((KK >> 2) * Layout::kKChunk + (KK & 3) * 32) >> 4;
+    constexpr uint32_t ob = ((KK >> 2) * Layout::kQChunk + (KK & 3) * 32) >> 4;
+    mma_ss_w<oa, ob>(d_s, klo, khi, qlo, qhi, idesc, KK > 0 ? 1u : 0u);
+    mma_ss_w<oa, ob>(d_dp, vlo, vhi, glo, ghi, idesc, KK > 0 ? 1u : 0u);
+    sdp_steps<KK + 1>(d_s, d_dp, klo, khi, vlo, vhi, qlo, qhi, glo, ghi, idesc);
+  }
+}
+// Unrolled K steps (64 queries in 16-wide steps) of dV += P^T dO and
+// dK += dS^T Q: A in TMEM (8 columns per step), B MN-major (2048 B per step).
+template <int KK>
+FA_DEV void grad_steps(uint32_t d_dv, uint32_t d_dk, uint32_t a_p, uint32_t a_ds, uint32_t golo, uint32_t gohi,
+                       uint32_t qlo, uint32_t qhi, uint32_t idesc, uint32_t acc) {
+  if constexpr (KK < kBM / 16) {
+    mma_ts_w<KK * 8, KK * 128>(d_dv, a_p, golo, gohi, idesc, KK > 0 ? 1u : acc);
+    mma_ts_w<KK * 8, KK * 128>(d_dk, a_ds, qlo, qhi, idesc, KK > 0 ? 1u : acc);
+    grad_steps<KK + 1>(d_dv, d_dk, a_p, a_ds, golo, gohi, qlo, qhi, idesc, acc);
+  }
+}
+// Unrolled K steps (128 keys in 16-wide steps) of dQ^T = K^T dS^T: both
+// operands MN-major, 16 key rows = 2048 B per step.
+template <int KK>
+FA_DEV void dq_steps(uint32_t d_dq, uint32_t klo, uint32_t khi, uint32_t slo, uint32_t shi, uint32_t idesc) {
+  if constexpr (KK < kBN / 16) {
+    mma_ss_w<KK * 128, KK * 128>(d_dq, klo, khi, slo, shi, idesc, KK > 0 ? 1u : 0u);
+    dq_steps<KK + 1>(d_dq, klo, khi, slo, shi, idesc);
+  }
+}
+
+// MMA issuer: the whole warp runs this, converged; an elected lane issues.
 __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   constexpr uint32_t kIdS = idesc_bf16_f32(kBN, kBM, false, false);   // S^T, dP^T: 128 keys x 64 queries
   constexpr uint32_t kIdG = idesc_bf16_f32(kBN, kD, false, true);     // dV, dK: A in TMEM, B MN-major
   constexpr uint32_t kIdQ = idesc_bf16_f32(kD, kBM, true, true);      // dQ^T: A = K^T, B = dS^T
   const uint32_t kb = sh.sbase + Layout::kK, vb = sh.sbase + Layout::kV;
+  const uint64_t dk_kmaj = sdesc_sw128(kb, 16, 1024), dv_kmaj = sdesc_sw128(vb, 16, 1024);
+  const uint64_t dk_mn = sdesc_sw128(kb, Layout::kKChunk, 1024);
   uint32_t sit = 0, ukv = 0;
 
   auto wait = [&](uint32_t bar, uint32_t parity, int site) -> bool {
@@ -267,18 +304,11 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
     tc_fence_after();
     return true;
   };
-  // S^T = K Q_i^T and dP^T = V dO_i^T (K-major operands, K = D in steps of 16)
   auto issue_sdp = [&](int st) {
-    const uint32_t qb = sh.stage(st), gb = qb + Layout::kQTile;
-    const uint64_t dk = sdesc_sw128(kb, 16, 1024), dv = sdesc_sw128(vb, 16, 1024);
-    const uint64_t dq = sdesc_sw128(qb, 16, 1024), dg = sdesc_sw128(gb, 16, 1024);
-#pragma unroll 1
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const uint32_t oa = ((kk >> 2) * Layout::kKChunk + (kk & 3) * 32) >> 4;
-      const uint32_t ob = ((kk >> 2) * Layout::kQChunk + (kk & 3) * 32) >> 4;
-      mma_ss(tmem + kColS, dk + oa, dq + ob, kIdS, kk > 0 ? 1u : 0u);
-      mma_ss(tmem + kColDP, dv + oa, dg + ob, kIdS, kk > 0 ? 1u : 0u);
-    }
+    const uint64_t dq = sdesc_sw128(sh.stage(st), 16, 1024);
+    const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout::kQTile, 16, 1024);
+    sdp_steps<0>(tmem + kColS, tmem + kColDP, desc_lo(dk_kmaj), desc_hi(dk_kmaj), desc_lo(dv_kmaj),
+                 desc_hi(dv_kmaj), desc_lo(dq), desc_hi(dq), desc_lo(dg), desc_hi(dg), kIdS);
   };
 
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
@@ -287,43 +317,35 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
     if (!wait(sh.kv_full(), ukv & 1, kSiteMmaKV)) return;
     if (!wait(sh.qd_full(sit % kStages), (sit / kStages) & 1, kSiteMmaQ)) return;
     issue_sdp(sit % kStages);
-    mma_commit(sh.s_full());
+    mma_commit_w(sh.s_full());
     for (int s = 0; s < w.steps; ++s, ++sit) {
       const int st = sit % kStages, buf = sit & 1;
       if (!wait(sh.p_ready(), sit & 1, kSiteMmaP)) return;
       if (s == 0 && ukv > 0 && !wait(sh.acc_empty(), (ukv - 1) & 1, kSiteMmaAcc)) return;
-      // dV += P^T dO_i, dK += dS^T Q_i: A from TMEM (8 columns per 16 queries),
-      // B MN-major (D contiguous, 64-wide chunks 8 KB apart, 16 queries = 2 KB)
+      // dV += P^T dO_i, dK += dS^T Q_i (B MN-major: D contiguous, 64-wide
+      // chunks 8 KB apart)
       const uint64_t dgo = sdesc_sw128(sh.stage(st) + Layout::kQTile, Layout::kQChunk, 1024);
       const uint64_t dqq = sdesc_sw128(sh.stage(st), Layout::kQChunk, 1024);
-#pragma unroll 1
-      for (int kk = 0; kk < kBM / 16; ++kk) {
-        const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-        mma_ts(tmem + kColDV, tmem + kColS + kk * 8, dgo + uint64_t(kk * (2048 >> 4)), kIdG, acc);
-        mma_ts(tmem + kColDK, tmem + kColDP + kk * 8, dqq + uint64_t(kk * (2048 >> 4)), kIdG, acc);
-      }
-      mma_commit(sh.qd_empty(st));
+      grad_steps<0>(tmem + kColDV, tmem + kColDK, tmem + kColS, tmem + kColDP, desc_lo(dgo), desc_hi(dgo),
+                    desc_lo(dqq), desc_hi(dqq), kIdG, s > 0 ? 1u : 0u);
+      mma_commit_w(sh.qd_empty(st));
       // next step's scores go ahead of this step's dQ product
       if (s + 1 < w.steps) {
         const uint32_t nx = sit + 1;
         if (!wait(sh.qd_full(nx % kStages), (nx / kStages) & 1, kSiteMmaQ)) return;
         issue_sdp(nx % kStages);
-        mma_commit(sh.s_full());
+        mma_commit_w(sh.s_full());
       }
       // dQ_i^T = K^T dS^T: M = D (K MN-major, chunks 16 KB apart), N = 64
-      // queries (dS^T MN-major), K = 128 keys in steps of 16 (2 KB)
+      // queries (dS^T MN-major), K = 128 keys
       if (!wait(sh.dq_empty(buf), ((sit >> 1) & 1) ^ 1, kSiteMmaDq)) return;
-      const uint64_t da = sdesc_sw128(kb, Layout::kKChunk, 1024);
-      const uint64_t db = sdesc_sw128(sh.ds(buf), Layout::kDsBytes, 1024);
-#pragma unroll 1
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_ss(tmem + kColDQ + buf * kBM, da + uint64_t(kk * (2048 >> 4)), db + uint64_t(kk * (2048 >> 4)), kIdQ,
-               kk > 0 ? 1u : 0u);
-      mma_commit(sh.dq_full(buf));
-      mma_commit(sh.ds_free(buf));
+      const uint64_t dsd = sdesc_sw128(sh.ds(buf), Layout::kDsBytes, 1024);
+      dq_steps<0>(tmem + kColDQ + buf * kBM, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd), kIdQ);
+      mma_commit_w(sh.dq_full(buf));
+      mma_commit_w(sh.ds_free(buf));
     }
-    mma_commit(sh.acc_full());
-    mma_commit(sh.kv_empty());
+    mma_commit_w(sh.acc_full());
+    mma_commit_w(sh.kv_empty());
     ++ukv;
   }
 }
@@ -590,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     if ((threadIdx.x % 32) == 0) producer_role(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
   } else if (warp == 9) {
-    if ((threadIdx.x % 32) == 0) mma_role(sh, tmem, p, total_units);
+    mma_role(sh, tmem, p, total_units);   // converged warp; one elected lane issues
   }
   if (ld_shared_volatile(sh.abort())) {
     const uint64_t t0 = globaltimer_ns();
