@@ -84,6 +84,20 @@ fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, i
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D,
+                                     int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)heads * D * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic) {
   BwdWorkspace w{};
   const size_t sq_pad = (size_t(Sq) + 63) / 64 * 64;

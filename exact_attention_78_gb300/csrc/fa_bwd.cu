@@ -15,9 +15,10 @@
 //             dV  += P^T dO_i           dK  += dS^T Q_i
 //             dQ_i^T = K^T dS^T   -> added to the FP32 accumulator
 //         dK and dV stay in TMEM across the whole group and are written once
-//         per unit, so they need no atomics.  dQ partial sums are added with
-//         FP32 reductions, or, in deterministic mode, in ascending key-block
-//         order enforced by one ticket per (batch, head, query block);
+//         per unit, so they need no atomics.  dQ partial sums are added by the
+//         TMA unit (bulk tensor reduce-add of a 64 x 128 FP32 tile per step),
+//         in deterministic mode in ascending key-block order enforced by one
+//         ticket per (batch, head, query block);
 //   post  dQ = BF16(scale * accumulator).
 //
 // Sources: "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
@@ -30,7 +31,7 @@
 //
 // Thread layout (384 threads, 12 warps, one CTA per SM):
 //   warps 0-3   P / dS elementwise warpgroup (one thread per key row)
-//   warps 4-7   dQ warpgroup (accumulator adds) and dK/dV epilogue
+//   warps 4-7   dQ warpgroup (TMA reduce-add of dQ tiles) and dK/dV epilogue
 //   warp  8     TMA producer (one lane)
 //   warp  9     TMEM owner + MMA issuer (converged warp, one elected lane issues)
 //   warps 10-11 idle
@@ -56,7 +57,7 @@ constexpr int kD = 128;        // head dimension of this kernel
 constexpr int kBN = 128;       // keys per work unit
 constexpr int kBM = 64;        // query rows per step
 constexpr int kThreads = 384;
-constexpr int kStages = 3;     // Q / dO ring depth
+constexpr int kStages = 2;     // Q / dO ring depth
 
 enum Site { kSiteEsS = 1, kSiteEsQ, kSiteEsDs, kSiteDqFull, kSiteDqTicket, kSiteAcc, kSiteMmaKV, kSiteMmaQ,
             kSiteMmaP, kSiteMmaDq, kSiteMmaAcc, kSiteProdKV, kSiteProdQ };
@@ -73,10 +74,12 @@ struct Layout {
   static constexpr int kStageStride = (kStageBytes + 1023) / 1024 * 1024;
   static constexpr int kDs = kStage0 + kStages * kStageStride;    // dS^T smem, 2 buffers of 16 KB
   static constexpr int kDsBytes = kBN * 128;
-  static constexpr int kBars = kDs + 2 * kDsBytes;
-  // kv_full, kv_empty, qd_full[3], qd_empty[3], s_full, p_ready,
-  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 6 + 2;
+  static constexpr int kDqStage = kDs + 2 * kDsBytes;             // FP32 dQ tile [64 rows][128]
+  static constexpr int kDqStageBytes = kBM * kD * 4;
+  static constexpr int kBars = kDqStage + kDqStageBytes;
+  // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full, p_ready,
+  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full, dqs_free
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 6 + 2 + 2;
   static constexpr int kMisc = kBars + kNumBars * 8;              // tmem slot, abort, check-in count
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kDynamic = kTotal + kSmemAlignSlack;
@@ -202,9 +205,12 @@ struct Shared {
   FA_DEV uint32_t ds_free(int b) const { return bar(8 + 2 * kStages + b); }
   FA_DEV uint32_t acc_full() const { return bar(10 + 2 * kStages); }
   FA_DEV uint32_t acc_empty() const { return bar(11 + 2 * kStages); }
+  FA_DEV uint32_t dqs_full() const { return bar(12 + 2 * kStages); }   // staging tile written (128 arrivals)
+  FA_DEV uint32_t dqs_free() const { return bar(13 + 2 * kStages); }   // staging tile read by the TMA unit
+  FA_DEV float* dq_stage() const { return reinterpret_cast<float*>(base + L::kDqStage); }
+  FA_DEV uint32_t dq_stage_addr() const { return sbase + L::kDqStage; }
   FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
   FA_DEV uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + L::kMisc); }
-  FA_DEV int* det_count() const { return reinterpret_cast<int*>(base + L::kMisc + 8); }
   FA_DEV uint32_t stage(int s) const { return sbase + L::kStage0 + s * L::kStageStride; }
   FA_DEV const float* stage_nlse2(int s) const {
     return reinterpret_cast<const float*>(base + L::kStage0 + s * L::kStageStride + 2 * L::kQTile);
@@ -427,18 +433,23 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
   }
 }
 
-// dQ warpgroup: thread = feature d; adds the 64 query columns of dQ_i^T to
-// the FP32 accumulator, then writes dK (scaled) and dV at the end of a unit.
-__device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
+// dQ warpgroup: thread = feature d.  Per step it moves dQ_i^T from TMEM to a
+// row-major FP32 tile [64 queries][128] in shared memory, and one thread adds
+// the tile into the FP32 accumulator with a single TMA bulk tensor
+// reduce-add (out-of-range rows are skipped by the unit; rows of a padded
+// query block that belong to the next sequence receive exact zeros, since
+// their weights are 0).  At the end of a unit it writes dK (scaled) and dV.
+__device__ void dq_role(const Shared& sh, const uint32_t tmem, const CUtensorMap* tdq, const BwdParams& p,
+                        const int total_units) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
   const int d = wq * 32 + lane;           // dQ^T lane = feature; dK/dV lane = key row
   const uint32_t tl = tmem + (uint32_t(wq * 32) << 16);
-  const int first = threadIdx.x == 128;   // first thread of this warpgroup
+  const bool first = threadIdx.x == 128;  // issues the reductions and handles tickets
   uint32_t sit = 0, ukv = 0;
-  int det_target = 0;                     // check-ins expected so far (deterministic mode)
   __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk);
   __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
+  float* stage = sh.dq_stage();
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit(u, p);
     for (int s = 0; s < w.steps; ++s, ++sit) {
@@ -446,7 +457,7 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
       const int i = w.i0 + s % w.nq;
       const int buf = sit & 1;
       if (!mbar_wait_bounded(sh.dq_full(buf), (sit >> 1) & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns))
-        return;
+        break;
       tc_fence_after();
       uint32_t v[2][32];
       tmem_ld32(tl + kColDQ + buf * kBM, v[0]);
@@ -456,72 +467,50 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
       tmem_ld_fence(v[1]);
       tc_fence_before();
       mbar_arrive(sh.dq_empty(buf));
-      // Deterministic mode: key blocks add into this (b, h, i) in ascending
-      // order n = 0, 1, ...  Every thread waits (bounded) for the ticket to
-      // reach n, adds, fences and checks in on a shared counter; the first
-      // thread waits (bounded) for all 128 check-ins and advances the ticket.
-      int* ticket = nullptr;
-      bool ok = true;
-      if (p.deterministic) {
-        ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(ticket) != w.n) {
-          if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
-            if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
-            st_shared(sh.abort(), 1);
-            ok = false;
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-      if (ok) {
-        const int q0 = kBM * i;
-        const int nvalid = min(kBM, p.Sq - q0);
-        float* base = p.dq_acc + ((size_t(w.b) * p.Sq + q0) * p.Hq + h) * kD + d;
-        const size_t rstride = size_t(p.Hq) * kD;
+      // the previous step's tile must have been read by the TMA unit
+      if (!mbar_wait_bounded(sh.dqs_free(), (sit & 1) ^ 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) break;
 #pragma unroll
-        for (int c = 0; c < kBM; ++c)
-          if (c < nvalid) atomicAdd(base + c * rstride, __uint_as_float(v[c / 32][c % 32]));
-      }
-      if (p.deterministic) {
-        if (!ok) return;
-        __threadfence();
-        atomicAdd(sh.det_count(), 1);
-        det_target += 128;
-        if (first) {
+      for (int c = 0; c < kBM; ++c) stage[c * kD + d] = __uint_as_float(v[c / 32][c % 32]);
+      fence_proxy_async_smem();
+      mbar_arrive(sh.dqs_full());
+      if (first) {
+        if (!mbar_wait_bounded(sh.dqs_full(), sit & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) break;
+        int* ticket = nullptr;
+        if (p.deterministic) {
+          // key blocks add into this (b, h, i) in ascending order n = 0, 1, ...
+          ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
           const uint64_t t0 = globaltimer_ns();
-          while (ld_shared_volatile(smem_u32(sh.det_count())) < det_target) {
+          bool ok = true;
+          while (ld_acquire_gpu(ticket) != w.n) {
             if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
               if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
               st_shared(sh.abort(), 1);
-              return;
-            }
-          }
-          __threadfence();
-          st_release_gpu(ticket, w.n + 1);
-        } else {
-          // hold until this step's ticket advanced, so no thread checks in
-          // for the next step before all have checked in for this one
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_acquire_gpu(ticket) == w.n) {
-            if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
-              if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
-              st_shared(sh.abort(), 1);
-              return;
+              ok = false;
+              break;
             }
             __nanosleep(64);
           }
+          if (!ok) break;
         }
+        tma_reduce_add_3d(tdq, sh.dq_stage_addr(), 0, h, w.b * p.Sq + kBM * i);
+        bulk_commit_group();
+        if (p.deterministic) {
+          bulk_wait_group0();          // the additions are performed ...
+          __threadfence();
+          st_release_gpu(ticket, w.n + 1);   // ... before the next key block may add
+        } else {
+          bulk_wait_group_read0();     // the tile may be overwritten
+        }
+        mbar_arrive(sh.dqs_free());
       }
-      if (!ok) return;
     }
+    if (ld_shared_volatile(sh.abort())) break;
     // epilogue of the unit: dV and scale * dK rows in BF16
     const int key = kBN * w.n + d;
     const bool valid = key < p.Sk;
     const size_t roff = ((size_t(w.b) * p.Sk + key) * p.Hkv + w.hk) * kD;
     if (w.steps > 0) {
-      if (!mbar_wait_bounded(sh.acc_full(), ukv & 1, sh.abort(), &g_err, kSiteAcc, p.wait_limit_ns)) return;
+      if (!mbar_wait_bounded(sh.acc_full(), ukv & 1, sh.abort(), &g_err, kSiteAcc, p.wait_limit_ns)) break;
       tc_fence_after();
     }
 #pragma unroll 1
@@ -558,12 +547,13 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
       ++ukv;
     }
   }
+  if (first) bulk_wait_group0();   // outstanding reductions finish before the CTA exits
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dqacc, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32;
@@ -586,8 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(sh.acc_full(), 1);
     mbar_init(sh.acc_empty(), 128);
+    mbar_init(sh.dqs_full(), 128);
+    mbar_init(sh.dqs_free(), 1);
     st_shared(sh.abort(), 0);
-    *sh.det_count() = 0;
     fence_barrier_init();
   }
   if (warp == 8 && (threadIdx.x % 32) == 0) {
@@ -595,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dqacc);
   }
   if (warp == 9) {
     tmem_alloc(sh.tmem_slot(), 512);
@@ -608,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     elementwise_role(sh, tmem, p, total_units);
   } else if (warp < 8) {
-    dq_role(sh, tmem, p, total_units);
+    dq_role(sh, tmem, &tm_dqacc, p, total_units);
   } else if (warp == 8) {
     if ((threadIdx.x % 32) == 0) producer_role(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
   } else if (warp == 9) {
@@ -631,8 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   const BwdParams& p = L.p;
   if (p.D != bwd::kD) return FA_ERR_UNSUPPORTED;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   fa_status st;
+  if ((st = make_tmap_f32_rows_heads_d(&tdq, p.dq_acc, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
   if ((st = make_tmap_rows_heads_d(&tq, L.q, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
   if ((st = make_tmap_rows_heads_d(&tdo, p.dout, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
   if ((st = make_tmap_rows_heads_d(&tk, L.k, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
@@ -658,7 +651,7 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   }
   const long long units = (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
   const int grid = (int)(units < L.num_sms ? units : L.num_sms);
-  bwd::bwd_kernel<<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, p);
+  bwd::bwd_kernel<<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
   // post: dQ = BF16(scale * accumulator)

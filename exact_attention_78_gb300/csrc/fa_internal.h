@@ -77,6 +77,10 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministi
 // 3-D tiled tensor map over a [rows, heads, D] BF16 array (D contiguous) with
 // a box of 64 x 1 x box_rows and 128-byte swizzle.
 fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_rows);
+// Same view over an FP32 [rows, heads, D] array, box D x 1 x box_rows, no
+// swizzle (a row-major staging tile).
+fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D,
+                                     int box_rows);
 
 // Kernel launchers (defined in their translation units).
 fa_status launch_fwd(const FwdLaunch& L, cudaStream_t stream);
