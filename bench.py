@@ -43,6 +43,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="dense", choices=["dense", "train", "varlen"],
+                    help="dense: B,H,S,D below; train: B=2 H=16 S=8192 D=128 causal; "
+                         "varlen: 64 packed sequences, Hq=32 Hkv=8, D=128, causal (forward only)")
+    ap.add_argument("--deterministic", action="store_true", help="deterministic dQ order in the backward")
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--fwd-only", action="store_true", help="time the forward call alone")
     ap.add_argument("--B", type=int, default=4)
@@ -141,6 +145,8 @@ def measured_traffic(kernel, w):
     for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             m.update(f.read())
+    if w.packed:
+        return None
     want = "dense B=%d Hq=Hkv=%d S=%d D=%d %s" % (w.B, w.Hq, w.Sq, w.D, "causal" if w.causal else "non-causal")
     if m.hexdigest()[:16] != rec["source_sha"] or rec["workload"] != want:
         return None
@@ -148,13 +154,22 @@ def measured_traffic(kernel, w):
 
 
 def workload(args):
+    if args.workload == "train":
+        return W.train(args.deterministic)
+    if args.workload == "varlen":
+        return W.varlen_gqa()
     return W.Workload("dense_causal" if args.causal else "dense", B=args.B, Hq=args.H, Hkv=args.H, Sq=args.S,
                       Sk=args.S, D=args.D, causal=args.causal)
 
 
+def fwd_flops_of(w):
+    if w.packed:
+        return F.varlen_fwd_flops(w.seqlens, w.Hq, w.D, w.causal)
+    return F.fwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
+
+
 def step_flops(w, with_bwd):
-    f = F.fwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
-    return f + (F.bwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal) if with_bwd else 0.0)
+    return fwd_flops_of(w) * (3.5 if with_bwd else 1.0)
 
 
 # --------------------------------------------------------------- oracle arm --
@@ -230,21 +245,25 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     fa.load_library(build_if_missing=(rank == 0))
     w = workload(args)
-    (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
+    (q, k, v, do), cu = W.make_inputs(w, with_grad=True)
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    cud = None if cu is None else cu.cuda()
     o = torch.empty_like(qd)
-    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device="cuda")
+    lse_shape = (w.Hq, qd.shape[0]) if w.packed else (w.B, w.Hq, w.Sq)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    det = bool(w.extra.get("deterministic", args.deterministic))
 
-    have_bwd = not args.fwd_only
+    have_bwd = not args.fwd_only and not w.packed
     ws_buf = dq = dk = dv = None
     if have_bwd:
         try:
-            need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, False)
+            need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, det)
             ws_buf = torch.empty(need, dtype=torch.uint8, device="cuda")
             dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
             fa.fwd(qd, kd, vd, causal=w.causal, out=o, lse=lse, emu_per_16=args.emu)
-            fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, workspace=ws_buf, dq=dq, dk=dk, dv=dv)
+            fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
+                   dv=dv)
         except fa.FAError as e:
             if e.status != 2:
                 raise
@@ -258,11 +277,12 @@ def run_gpu(args):
     def step(i=None):
         if i is not None:
             ev_f0[i].record(stream)
-        fa.fwd(qd, kd, vd, causal=w.causal, out=o, lse=lse, emu_per_16=args.emu)
+        fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, emu_per_16=args.emu)
         if i is not None:
             ev_f1[i].record(stream)
         if have_bwd:
-            fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, workspace=ws_buf, dq=dq, dk=dk, dv=dv)
+            fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
+                   dv=dv)
         if i is not None:
             ev_b1[i].record(stream)
 
@@ -349,9 +369,9 @@ def run_gpu(args):
     pk, pk_kind = peaks()
     # dominant kernel: the longer of the forward kernel and the backward call
     if have_bwd and bwd_ms > fwd_ms:
-        dom, dom_ms, dom_flops = "bwd", bwd_ms, F.bwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
+        dom, dom_ms, dom_flops = "bwd", bwd_ms, 2.5 * fwd_flops_of(w)
     else:
-        dom, dom_ms, dom_flops = "fwd", fwd_ms, F.fwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal)
+        dom, dom_ms, dom_flops = "fwd", fwd_ms, fwd_flops_of(w)
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -366,13 +386,12 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**w.describe(), "step": "fwd+bwd" if have_bwd else "fwd",
+        "config": {**w.describe(), "step": "fwd+bwd" if have_bwd else "fwd", "deterministic": det,
                    "l2": "inputs larger than L2 (Q,K,V,O %d MiB each)" % (qd.numel() * 2 >> 20),
                    "parallelism": "replicas" if ws > 1 else "single"},
-        "fwd_tflops": F.fwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal) / (fwd_ms * 1e-3) / 1e12,
+        "fwd_tflops": fwd_flops_of(w) / (fwd_ms * 1e-3) / 1e12,
         "fwd_ms": fwd_ms,
-        "bwd_tflops": (F.bwd_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal) / (bwd_ms * 1e-3) / 1e12
-                       if have_bwd else None),
+        "bwd_tflops": (2.5 * fwd_flops_of(w) / (bwd_ms * 1e-3) / 1e12 if have_bwd else None),
         "bwd_ms": bwd_ms if have_bwd else None,
         "roofline": roofline,
         "cpu_baseline": cpu,
