@@ -32,6 +32,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from exact_attention_78_gb300 import flops as F  # noqa: E402
+from exact_attention_78_gb300 import replicas  # noqa: E402
 from exact_attention_78_gb300 import workloads as W  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOPS on 1 GB300, BF16 D=128 S=1K–32K; % of BF16 peak"
@@ -60,10 +61,7 @@ def parse():
 
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return replicas.rank_env()
 
 
 def peaks():
@@ -241,8 +239,7 @@ def run_gpu(args):
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)
     if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        replicas.init("nccl", device=torch.device("cuda", local))
     fa.load_library(build_if_missing=(rank == 0))
     w = workload(args)
     (q, k, v, do), cu = W.make_inputs(w, with_grad=True)
@@ -294,8 +291,7 @@ def run_gpu(args):
 
     def barrier():
         torch.cuda.synchronize()
-        if ws > 1:
-            torch.distributed.barrier()
+        replicas.barrier()
         torch.cuda.synchronize()
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -309,11 +305,7 @@ def run_gpu(args):
     barrier()
     if fa.get_device_error() != 0:
         raise RuntimeError("device error in timed region")
-    elapsed_ms = start.elapsed_time(end)
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t)
+    elapsed_ms = replicas.max_over_ranks(start.elapsed_time(end), device="cuda")
     fwd_ms = statistics.mean(ev_f0[i].elapsed_time(ev_f1[i]) for i in range(args.steps))
     bwd_ms = statistics.mean(ev_f1[i].elapsed_time(ev_b1[i]) for i in range(args.steps)) if have_bwd else 0.0
 
@@ -353,17 +345,12 @@ def run_gpu(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1) / n_e2e
-        if ws > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t)
+        e_ms = replicas.max_over_ranks(e0.elapsed_time(e1) / n_e2e, device="cuda")
         e2e = {"value": ws * flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
     if rank != 0:
-        if ws > 1:
-            torch.distributed.destroy_process_group()
+        replicas.finalize()
         return
 
     pk, pk_kind = peaks()
@@ -400,8 +387,7 @@ def run_gpu(args):
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
-    if ws > 1:
-        torch.distributed.destroy_process_group()
+    replicas.finalize()
 
 
 def main():
