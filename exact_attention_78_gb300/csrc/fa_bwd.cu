@@ -16,7 +16,7 @@
 //             dQ_i^T = K^T dS^T   -> added to the FP32 accumulator
 //         dK and dV stay in TMEM across the whole group and are written once
 //         per unit, so they need no atomics.  dQ partial sums are added by the
-//         TMA unit (bulk tensor reduce-add of a 64 x 128 FP32 tile per step),
+//         TMA unit (bulk tensor reduce-adds of 32 x 128 FP32 tiles),
 //         in deterministic mode in ascending key-block order enforced by one
 //         ticket per (batch, head, query block);
 //   post  dQ = BF16(scale * accumulator).
@@ -57,7 +57,8 @@ constexpr int kD = 128;        // head dimension of this kernel
 constexpr int kBN = 128;       // keys per work unit
 constexpr int kBM = 64;        // query rows per step
 constexpr int kThreads = 384;
-constexpr int kStages = 2;     // Q / dO ring depth
+constexpr int kStages = 3;     // Q / dO ring depth
+constexpr int kDqRows = 32;    // rows of the FP32 dQ staging tile (half a query block)
 
 enum Site { kSiteEsS = 1, kSiteEsQ, kSiteEsDs, kSiteDqFull, kSiteDqTicket, kSiteAcc, kSiteMmaKV, kSiteMmaQ,
             kSiteMmaP, kSiteMmaDq, kSiteMmaAcc, kSiteProdKV, kSiteProdQ };
@@ -74,12 +75,12 @@ struct Layout {
   static constexpr int kStageStride = (kStageBytes + 1023) / 1024 * 1024;
   static constexpr int kDs = kStage0 + kStages * kStageStride;    // dS^T smem, 2 buffers of 16 KB
   static constexpr int kDsBytes = kBN * 128;
-  static constexpr int kDqStage = kDs + 2 * kDsBytes;             // FP32 dQ tile [64 rows][128]
-  static constexpr int kDqStageBytes = kBM * kD * 4;
+  static constexpr int kDqStage = kDs + 2 * kDsBytes;             // FP32 dQ tile [32 rows][128]
+  static constexpr int kDqStageBytes = kDqRows * kD * 4;
   static constexpr int kBars = kDqStage + kDqStageBytes;
-  // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full, p_ready,
+  // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full[2], p_ready[2],
   // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full, dqs_free
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 6 + 2 + 2;
+  static constexpr int kNumBars = 2 + 2 * kStages + 10 + 4;
   static constexpr int kMisc = kBars + kNumBars * 8;              // tmem slot, abort, check-in count
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kDynamic = kTotal + kSmemAlignSlack;
@@ -171,8 +172,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p) {
   // ascending order: under a causal mask the early blocks see the most query
   // rows, so each head's longest units come first.
   const int nkv = (p.Sk + kBN - 1) / kBN;
-  const int bh = u / nkv;
-  w.n = u % nkv;
+  int bh;
+  if (p.deterministic) {
+    // Deterministic mode orders each (b, h, query block)'s dQ additions by key
+    // block; key-block-major units put a block's predecessor in an earlier
+    // wave of the grid, so the ordered additions rarely wait.
+    bh = u % (p.B * p.Hkv);
+    w.n = u / (p.B * p.Hkv);
+  } else {
+    bh = u / nkv;
+    w.n = u % nkv;
+  }
   w.b = bh / p.Hkv;
   w.hk = bh % p.Hkv;
   const int nqb = (p.Sq + kBM - 1) / kBM;
@@ -198,15 +208,17 @@ struct Shared {
   FA_DEV uint32_t kv_empty() const { return bar(1); }
   FA_DEV uint32_t qd_full(int s) const { return bar(2 + s); }
   FA_DEV uint32_t qd_empty(int s) const { return bar(2 + kStages + s); }
-  FA_DEV uint32_t s_full() const { return bar(2 + 2 * kStages); }
-  FA_DEV uint32_t p_ready() const { return bar(3 + 2 * kStages); }
-  FA_DEV uint32_t dq_full(int b) const { return bar(4 + 2 * kStages + b); }
-  FA_DEV uint32_t dq_empty(int b) const { return bar(6 + 2 * kStages + b); }
-  FA_DEV uint32_t ds_free(int b) const { return bar(8 + 2 * kStages + b); }
-  FA_DEV uint32_t acc_full() const { return bar(10 + 2 * kStages); }
-  FA_DEV uint32_t acc_empty() const { return bar(11 + 2 * kStages); }
-  FA_DEV uint32_t dqs_full() const { return bar(12 + 2 * kStages); }   // staging tile written (128 arrivals)
-  FA_DEV uint32_t dqs_free() const { return bar(13 + 2 * kStages); }   // staging tile read by the TMA unit
+  // per TMEM score buffer b (steps alternate buffers)
+  FA_DEV uint32_t s_full(int b) const { return bar(2 + 2 * kStages + b); }
+  FA_DEV uint32_t p_ready(int b) const { return bar(4 + 2 * kStages + b); }
+  FA_DEV uint32_t dq_full(int b) const { return bar(6 + 2 * kStages + b); }
+  FA_DEV uint32_t dq_empty(int b) const { return bar(8 + 2 * kStages + b); }
+  // per shared-memory dS buffer
+  FA_DEV uint32_t ds_free(int b) const { return bar(10 + 2 * kStages + b); }
+  FA_DEV uint32_t acc_full() const { return bar(12 + 2 * kStages); }
+  FA_DEV uint32_t acc_empty() const { return bar(13 + 2 * kStages); }
+  FA_DEV uint32_t dqs_full() const { return bar(14 + 2 * kStages); }   // staging tile written (128 arrivals)
+  FA_DEV uint32_t dqs_free() const { return bar(15 + 2 * kStages); }   // staging tile read by the TMA unit
   FA_DEV float* dq_stage() const { return reinterpret_cast<float*>(base + L::kDqStage); }
   FA_DEV uint32_t dq_stage_addr() const { return sbase + L::kDqStage; }
   FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
@@ -220,8 +232,10 @@ struct Shared {
   FA_DEV uint8_t* ds_ptr(int b) const { return base + L::kDs + b * L::kDsBytes; }
 };
 
-// TMEM columns
-constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDK = 256, kColDQ = 384;
+// TMEM columns.  Two score buffers b = 0, 1 (steps alternate): S^T at
+// 128 b, dP^T at 128 b + 64.  After a step's P^T / dS^T have been consumed,
+// its dQ^T product is written over the S^T columns of the same buffer.
+constexpr uint32_t kColBuf = 128, kColDPoff = 64, kColDV = 256, kColDK = 384;
 
 __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv, const CUtensorMap* tdo, const BwdParams& p,
@@ -310,43 +324,47 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
     tc_fence_after();
     return true;
   };
-  auto issue_sdp = [&](int st) {
+  auto issue_sdp = [&](int st, int buf) {
     const uint64_t dq = sdesc_sw128(sh.stage(st), 16, 1024);
     const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout::kQTile, 16, 1024);
-    sdp_steps<0>(tmem + kColS, tmem + kColDP, desc_lo(dk_kmaj), desc_hi(dk_kmaj), desc_lo(dv_kmaj),
-                 desc_hi(dv_kmaj), desc_lo(dq), desc_hi(dq), desc_lo(dg), desc_hi(dg), kIdS);
+    sdp_steps<0>(tmem + kColBuf * buf, tmem + kColBuf * buf + kColDPoff, desc_lo(dk_kmaj), desc_hi(dk_kmaj),
+                 desc_lo(dv_kmaj), desc_hi(dv_kmaj), desc_lo(dq), desc_hi(dq), desc_lo(dg), desc_hi(dg), kIdS);
+  };
+  // Scores of global step t into buffer t & 1, once the dQ^T written there
+  // by step t - 2 has been read out.
+  auto scores = [&](uint32_t t) -> bool {
+    const int buf = t & 1;
+    if (!wait(sh.qd_full(t % kStages), (t / kStages) & 1, kSiteMmaQ)) return false;
+    if (!wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
+    issue_sdp(t % kStages, buf);
+    mma_commit_w(sh.s_full(buf));
+    return true;
   };
 
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit(u, p);
     if (w.steps == 0) continue;
     if (!wait(sh.kv_full(), ukv & 1, kSiteMmaKV)) return;
-    if (!wait(sh.qd_full(sit % kStages), (sit / kStages) & 1, kSiteMmaQ)) return;
-    issue_sdp(sit % kStages);
-    mma_commit_w(sh.s_full());
+    if (!scores(sit)) return;
     for (int s = 0; s < w.steps; ++s, ++sit) {
       const int st = sit % kStages, buf = sit & 1;
-      if (!wait(sh.p_ready(), sit & 1, kSiteMmaP)) return;
+      // next step's scores first, so they are computed while the
+      // elementwise pass of this step runs
+      if (s + 1 < w.steps && !scores(sit + 1)) return;
+      if (!wait(sh.p_ready(buf), (sit >> 1) & 1, kSiteMmaP)) return;
       if (s == 0 && ukv > 0 && !wait(sh.acc_empty(), (ukv - 1) & 1, kSiteMmaAcc)) return;
       // dV += P^T dO_i, dK += dS^T Q_i (B MN-major: D contiguous, 64-wide
       // chunks 8 KB apart)
       const uint64_t dgo = sdesc_sw128(sh.stage(st) + Layout::kQTile, Layout::kQChunk, 1024);
       const uint64_t dqq = sdesc_sw128(sh.stage(st), Layout::kQChunk, 1024);
-      grad_steps<0>(tmem + kColDV, tmem + kColDK, tmem + kColS, tmem + kColDP, desc_lo(dgo), desc_hi(dgo),
-                    desc_lo(dqq), desc_hi(dqq), kIdG, s > 0 ? 1u : 0u);
+      grad_steps<0>(tmem + kColDV, tmem + kColDK, tmem + kColBuf * buf, tmem + kColBuf * buf + kColDPoff,
+                    desc_lo(dgo), desc_hi(dgo), desc_lo(dqq), desc_hi(dqq), kIdG, s > 0 ? 1u : 0u);
       mma_commit_w(sh.qd_empty(st));
-      // next step's scores go ahead of this step's dQ product
-      if (s + 1 < w.steps) {
-        const uint32_t nx = sit + 1;
-        if (!wait(sh.qd_full(nx % kStages), (nx / kStages) & 1, kSiteMmaQ)) return;
-        issue_sdp(nx % kStages);
-        mma_commit_w(sh.s_full());
-      }
-      // dQ_i^T = K^T dS^T: M = D (K MN-major, chunks 16 KB apart), N = 64
-      // queries (dS^T MN-major), K = 128 keys
-      if (!wait(sh.dq_empty(buf), ((sit >> 1) & 1) ^ 1, kSiteMmaDq)) return;
+      // dQ_i^T = K^T dS^T over the S^T columns of this buffer (its P^T has
+      // just been read by the dV product, issued before): M = D (K MN-major,
+      // chunks 16 KB apart), N = 64 queries (dS^T MN-major), K = 128 keys
       const uint64_t dsd = sdesc_sw128(sh.ds(buf), Layout::kDsBytes, 1024);
-      dq_steps<0>(tmem + kColDQ + buf * kBM, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd), kIdQ);
+      dq_steps<0>(tmem + kColBuf * buf, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd), kIdQ);
       mma_commit_w(sh.dq_full(buf));
       mma_commit_w(sh.ds_free(buf));
     }
@@ -375,13 +393,15 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
       const int st = sit % kStages, buf = sit & 1;
       if (!mbar_wait_bounded(sh.qd_full(st), (sit / kStages) & 1, sh.abort(), &g_err, kSiteEsQ, p.wait_limit_ns))
         return;
-      if (!mbar_wait_bounded(sh.s_full(), sit & 1, sh.abort(), &g_err, kSiteEsS, p.wait_limit_ns)) return;
+      if (!mbar_wait_bounded(sh.s_full(buf), (sit >> 1) & 1, sh.abort(), &g_err, kSiteEsS, p.wait_limit_ns))
+        return;
       tc_fence_after();
+      const uint32_t tb = tl + kColBuf * buf;
       uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tl + kColS, sr[0]);
-      tmem_ld32(tl + kColS + 32, sr[1]);
-      tmem_ld32(tl + kColDP, dr[0]);
-      tmem_ld32(tl + kColDP + 32, dr[1]);
+      tmem_ld32(tb, sr[0]);
+      tmem_ld32(tb + 32, sr[1]);
+      tmem_ld32(tb + kColDPoff, dr[0]);
+      tmem_ld32(tb + kColDPoff + 32, dr[1]);
       tmem_ld_wait();
       tmem_ld_fence(sr[0]);
       tmem_ld_fence(sr[1]);
@@ -413,8 +433,8 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
         dd[c / 2] = pack_bf16x2(s0, s1);
       }
       // P^T and dS^T as BF16 into TMEM (A operands of dV and dK)
-      tmem_st32(tl + kColS, pp);
-      tmem_st32(tl + kColDP, dd);
+      tmem_st32(tb, pp);
+      tmem_st32(tb + kColDPoff, dd);
       // dS^T into shared memory (B operand of dQ^T): row kr, 128-byte rows,
       // 16-byte chunk j stored at chunk j ^ (kr mod 8)
       if (!mbar_wait_bounded(sh.ds_free(buf), ((sit >> 1) & 1) ^ 1, sh.abort(), &g_err, kSiteEsDs,
@@ -428,15 +448,15 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(sh.p_ready());
+      mbar_arrive(sh.p_ready(buf));
     }
   }
 }
 
 // dQ warpgroup: thread = feature d.  Per step it moves dQ_i^T from TMEM to a
-// row-major FP32 tile [64 queries][128] in shared memory, and one thread adds
-// the tile into the FP32 accumulator with a single TMA bulk tensor
-// reduce-add (out-of-range rows are skipped by the unit; rows of a padded
+// row-major FP32 staging tile in shared memory (two halves of 32 queries x
+// 128), and one thread adds each half into the FP32 accumulator with a TMA
+// bulk tensor reduce-add (out-of-range rows are skipped by the unit; rows of a padded
 // query block that belong to the next sequence receive exact zeros, since
 // their weights are 0).  At the end of a unit it writes dK (scaled) and dV.
 __device__ void dq_role(const Shared& sh, const uint32_t tmem, const CUtensorMap* tdq, const BwdParams& p,
@@ -460,49 +480,62 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const CUtensorMap
         break;
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(tl + kColDQ + buf * kBM, v[0]);
-      tmem_ld32(tl + kColDQ + buf * kBM + 32, v[1]);
+      tmem_ld32(tl + kColBuf * buf, v[0]);
+      tmem_ld32(tl + kColBuf * buf + 32, v[1]);
       tmem_ld_wait();
       tmem_ld_fence(v[0]);
       tmem_ld_fence(v[1]);
       tc_fence_before();
       mbar_arrive(sh.dq_empty(buf));
-      // the previous step's tile must have been read by the TMA unit
-      if (!mbar_wait_bounded(sh.dqs_free(), (sit & 1) ^ 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) break;
+      // Two half tiles of 32 rows through one staging buffer; each is added
+      // by one TMA reduce once every thread has written its column.
+      int* ticket = nullptr;
+      bool stop = false;
 #pragma unroll
-      for (int c = 0; c < kBM; ++c) stage[c * kD + d] = __uint_as_float(v[c / 32][c % 32]);
-      fence_proxy_async_smem();
-      mbar_arrive(sh.dqs_full());
-      if (first) {
-        if (!mbar_wait_bounded(sh.dqs_full(), sit & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) break;
-        int* ticket = nullptr;
-        if (p.deterministic) {
-          // key blocks add into this (b, h, i) in ascending order n = 0, 1, ...
-          ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
-          const uint64_t t0 = globaltimer_ns();
-          bool ok = true;
-          while (ld_acquire_gpu(ticket) != w.n) {
-            if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
-              if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
-              st_shared(sh.abort(), 1);
-              ok = false;
-              break;
-            }
-            __nanosleep(64);
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t hs = 2 * sit + half;   // half-tile counter (staging phases)
+        if (!mbar_wait_bounded(sh.dqs_free(), (hs & 1) ^ 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) {
+          stop = true;
+          break;
+        }
+#pragma unroll
+        for (int c = 0; c < kDqRows; ++c)
+          stage[c * kD + d] = __uint_as_float(v[half][c]);
+        fence_proxy_async_smem();
+        mbar_arrive(sh.dqs_full());
+        if (first) {
+          if (!mbar_wait_bounded(sh.dqs_full(), hs & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) {
+            stop = true;
+            break;
           }
-          if (!ok) break;
+          if (p.deterministic && half == 0) {
+            // key blocks add into this (b, h, i) in ascending order n = 0, 1, ...
+            ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(ticket) != w.n) {
+              if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
+                if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
+                st_shared(sh.abort(), 1);
+                stop = true;
+                break;
+              }
+              __nanosleep(64);
+            }
+            if (stop) break;
+          }
+          tma_reduce_add_3d(tdq, sh.dq_stage_addr(), 0, h, w.b * p.Sq + kBM * i + kDqRows * half);
+          bulk_commit_group();
+          if (p.deterministic && half == 1) {
+            bulk_wait_group0();              // both halves are added ...
+            __threadfence();
+            st_release_gpu(ticket, w.n + 1);  // ... before the next key block may add
+          } else {
+            bulk_wait_group_read0();         // the staging tile may be overwritten
+          }
+          mbar_arrive(sh.dqs_free());
         }
-        tma_reduce_add_3d(tdq, sh.dq_stage_addr(), 0, h, w.b * p.Sq + kBM * i);
-        bulk_commit_group();
-        if (p.deterministic) {
-          bulk_wait_group0();          // the additions are performed ...
-          __threadfence();
-          st_release_gpu(ticket, w.n + 1);   // ... before the next key block may add
-        } else {
-          bulk_wait_group_read0();     // the tile may be overwritten
-        }
-        mbar_arrive(sh.dqs_free());
       }
+      if (stop) break;
     }
     if (ld_shared_volatile(sh.abort())) break;
     // epilogue of the unit: dV and scale * dK rows in BF16
@@ -567,9 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sh.qd_full(s), 1);
       mbar_init(sh.qd_empty(s), 1);
     }
-    mbar_init(sh.s_full(), 1);
-    mbar_init(sh.p_ready(), 128);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(sh.s_full(b), 1);
+      mbar_init(sh.p_ready(b), 128);
       mbar_init(sh.dq_full(b), 1);
       mbar_init(sh.dq_empty(b), 128);
       mbar_init(sh.ds_free(b), 1);
@@ -625,7 +658,7 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   if (p.D != bwd::kD) return FA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv, tdo, tdq;
   fa_status st;
-  if ((st = make_tmap_f32_rows_heads_d(&tdq, p.dq_acc, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
+  if ((st = make_tmap_f32_rows_heads_d(&tdq, p.dq_acc, p.B * p.Sq, p.Hq, p.D, bwd::kDqRows)) != FA_OK) return st;
   if ((st = make_tmap_rows_heads_d(&tq, L.q, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
   if ((st = make_tmap_rows_heads_d(&tdo, p.dout, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
   if ((st = make_tmap_rows_heads_d(&tk, L.k, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
