@@ -16,9 +16,10 @@
 //             dQ_i^T = K^T dS^T   -> added to the FP32 accumulator
 //         dK and dV stay in TMEM across the whole group and are written once
 //         per unit, so they need no atomics.  dQ partial sums are added by the
-//         TMA unit (bulk tensor reduce-adds of 32 x 128 FP32 tiles),
-//         in deterministic mode in ascending key-block order enforced by one
-//         ticket per (batch, head, query block);
+//         TMA unit (bulk tensor reduce-adds of 32 x 128 FP32 tiles staged
+//         through two shared-memory buffers, so one tile is written while the
+//         other is read), in deterministic mode in ascending key-block order
+//         enforced by one ticket per (batch, head, query block);
 //   post  dQ = BF16(scale * accumulator).
 //
 // Sources: "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
@@ -31,10 +32,12 @@
 //
 // Thread layout (384 threads, 12 warps, one CTA per SM):
 //   warps 0-3   P / dS elementwise warpgroup (one thread per key row)
-//   warps 4-7   dQ warpgroup (TMA reduce-add of dQ tiles) and dK/dV epilogue
+//   warps 4-7   dQ warpgroup (dQ^T from TMEM to the staging tiles) and the
+//               dK/dV epilogue
 //   warp  8     TMA producer (one lane)
 //   warp  9     TMEM owner + MMA issuer (converged warp, one elected lane issues)
-//   warps 10-11 idle
+//   warp  10    dQ reduce issuer (one lane; deterministic-mode tickets)
+//   warp  11    idle
 //
 // Tensor memory (512 columns): S^T [0,64) (P^T as BF16 in [0,32)),
 // dP^T [64,128) (dS^T as BF16 in [64,96)), dV [128,256), dK [256,384),
@@ -68,19 +71,20 @@ struct Layout {
   static constexpr int kKChunk = kBN * 128;          // 16 KB
   static constexpr int kQTile = kBM * kD * 2;        // 16 KB, 2 chunks of 64 rows x 128 B
   static constexpr int kQChunk = kBM * 128;          // 8 KB
-  static constexpr int kStageBytes = 2 * kQTile + 2 * kBM * 4;   // Q, dO, lse2, delta
+  static constexpr int kStageStride = 2 * kQTile;                 // Q, dO (1024-aligned)
+  static constexpr int kRowTermBytes = 2 * kBM * 4;               // -LSE2, -Delta of the stage's rows
   static constexpr int kK = 0;
   static constexpr int kV = kK + kKTile;
-  static constexpr int kStage0 = kV + kKTile;                     // 1024-aligned
-  static constexpr int kStageStride = (kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kStage0 = kV + kKTile;
   static constexpr int kDs = kStage0 + kStages * kStageStride;    // dS^T smem, 2 buffers of 16 KB
   static constexpr int kDsBytes = kBN * 128;
-  static constexpr int kDqStage = kDs + 2 * kDsBytes;             // FP32 dQ tile [32 rows][128]
+  static constexpr int kDqStage = kDs + 2 * kDsBytes;             // 2 FP32 dQ tiles [32 rows][128]
   static constexpr int kDqStageBytes = kDqRows * kD * 4;
-  static constexpr int kBars = kDqStage + kDqStageBytes;
+  static constexpr int kRowTerms = kDqStage + 2 * kDqStageBytes;  // [kStages][2][kBM] floats
+  static constexpr int kBars = kRowTerms + kStages * kRowTermBytes;
   // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full[2], p_ready[2],
-  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full, dqs_free
-  static constexpr int kNumBars = 2 + 2 * kStages + 10 + 4;
+  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full[2], dqs_free[2]
+  static constexpr int kNumBars = 2 + 2 * kStages + 10 + 2 + 4;
   static constexpr int kMisc = kBars + kNumBars * 8;              // tmem slot, abort, check-in count
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kDynamic = kTotal + kSmemAlignSlack;
@@ -217,15 +221,19 @@ struct Shared {
   FA_DEV uint32_t ds_free(int b) const { return bar(10 + 2 * kStages + b); }
   FA_DEV uint32_t acc_full() const { return bar(12 + 2 * kStages); }
   FA_DEV uint32_t acc_empty() const { return bar(13 + 2 * kStages); }
-  FA_DEV uint32_t dqs_full() const { return bar(14 + 2 * kStages); }   // staging tile written (128 arrivals)
-  FA_DEV uint32_t dqs_free() const { return bar(15 + 2 * kStages); }   // staging tile read by the TMA unit
-  FA_DEV float* dq_stage() const { return reinterpret_cast<float*>(base + L::kDqStage); }
-  FA_DEV uint32_t dq_stage_addr() const { return sbase + L::kDqStage; }
+  // per dQ staging tile (half a query block each)
+  FA_DEV uint32_t dqs_full(int b) const { return bar(14 + 2 * kStages + b); }   // written (128 arrivals)
+  FA_DEV uint32_t dqs_free(int b) const { return bar(16 + 2 * kStages + b); }   // read by the TMA unit
+  FA_DEV float* dq_stage(int b) const {
+    return reinterpret_cast<float*>(base + L::kDqStage + b * L::kDqStageBytes);
+  }
+  FA_DEV uint32_t dq_stage_addr(int b) const { return sbase + L::kDqStage + b * L::kDqStageBytes; }
   FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
   FA_DEV uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + L::kMisc); }
   FA_DEV uint32_t stage(int s) const { return sbase + L::kStage0 + s * L::kStageStride; }
+  FA_DEV uint32_t row_terms(int s) const { return sbase + L::kRowTerms + s * L::kRowTermBytes; }
   FA_DEV const float* stage_nlse2(int s) const {
-    return reinterpret_cast<const float*>(base + L::kStage0 + s * L::kStageStride + 2 * L::kQTile);
+    return reinterpret_cast<const float*>(base + L::kRowTerms + s * L::kRowTermBytes);
   }
   FA_DEV const float* stage_ndelta(int s) const { return stage_nlse2(s) + kBM; }
   FA_DEV uint32_t ds(int b) const { return sbase + L::kDs + b * L::kDsBytes; }
@@ -268,8 +276,8 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
         tma_load_3d(sb + Layout::kQTile + c * Layout::kQChunk, tdo, sh.qd_full(st), c * 64, h, qrow);
       }
       const size_t roff = (size_t(w.b) * p.Hq + h) * p.sq_pad + size_t(kBM) * i;
-      bulk_load(sb + 2 * Layout::kQTile, p.nlse2 + roff, kBM * 4, sh.qd_full(st));
-      bulk_load(sb + 2 * Layout::kQTile + kBM * 4, p.ndelta + roff, kBM * 4, sh.qd_full(st));
+      bulk_load(sh.row_terms(st), p.nlse2 + roff, kBM * 4, sh.qd_full(st));
+      bulk_load(sh.row_terms(st) + kBM * 4, p.ndelta + roff, kBM * 4, sh.qd_full(st));
     }
     ++ukv;
   }
@@ -453,31 +461,27 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
   }
 }
 
-// dQ warpgroup: thread = feature d.  Per step it moves dQ_i^T from TMEM to a
-// row-major FP32 staging tile in shared memory (two halves of 32 queries x
-// 128), and one thread adds each half into the FP32 accumulator with a TMA
-// bulk tensor reduce-add (out-of-range rows are skipped by the unit; rows of a padded
-// query block that belong to the next sequence receive exact zeros, since
-// their weights are 0).  At the end of a unit it writes dK (scaled) and dV.
-__device__ void dq_role(const Shared& sh, const uint32_t tmem, const CUtensorMap* tdq, const BwdParams& p,
-                        const int total_units) {
+// dQ warpgroup: thread = feature d.  Per step it moves dQ_i^T from TMEM to the
+// two row-major FP32 staging tiles in shared memory (queries 0-31 and 32-63
+// of the block, 32 x 128 each); the reduce issuer adds each into the FP32
+// accumulator.  At the end of a unit it writes dK (scaled) and dV.
+__device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
   const int d = wq * 32 + lane;           // dQ^T lane = feature; dK/dV lane = key row
   const uint32_t tl = tmem + (uint32_t(wq * 32) << 16);
-  const bool first = threadIdx.x == 128;  // issues the reductions and handles tickets
   uint32_t sit = 0, ukv = 0;
   __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk);
   __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
-  float* stage = sh.dq_stage();
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit(u, p);
+    bool stop = false;
     for (int s = 0; s < w.steps; ++s, ++sit) {
-      const int h = w.hk * p.group + s / w.nq;
-      const int i = w.i0 + s % w.nq;
       const int buf = sit & 1;
-      if (!mbar_wait_bounded(sh.dq_full(buf), (sit >> 1) & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns))
+      if (!mbar_wait_bounded(sh.dq_full(buf), (sit >> 1) & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) {
+        stop = true;
         break;
+      }
       tc_fence_after();
       uint32_t v[2][32];
       tmem_ld32(tl + kColBuf * buf, v[0]);
@@ -487,57 +491,23 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const CUtensorMap
       tmem_ld_fence(v[1]);
       tc_fence_before();
       mbar_arrive(sh.dq_empty(buf));
-      // Two half tiles of 32 rows through one staging buffer; each is added
-      // by one TMA reduce once every thread has written its column.
-      int* ticket = nullptr;
-      bool stop = false;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const uint32_t hs = 2 * sit + half;   // half-tile counter (staging phases)
-        if (!mbar_wait_bounded(sh.dqs_free(), (hs & 1) ^ 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) {
+        // tile `half` of step sit is the sit-th use of that buffer
+        if (!mbar_wait_bounded(sh.dqs_free(half), (sit & 1) ^ 1, sh.abort(), &g_err, kSiteDqFull,
+                               p.wait_limit_ns)) {
           stop = true;
           break;
         }
+        float* stage = sh.dq_stage(half);
 #pragma unroll
-        for (int c = 0; c < kDqRows; ++c)
-          stage[c * kD + d] = __uint_as_float(v[half][c]);
+        for (int c = 0; c < kDqRows; ++c) stage[c * kD + d] = __uint_as_float(v[half][c]);
         fence_proxy_async_smem();
-        mbar_arrive(sh.dqs_full());
-        if (first) {
-          if (!mbar_wait_bounded(sh.dqs_full(), hs & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) {
-            stop = true;
-            break;
-          }
-          if (p.deterministic && half == 0) {
-            // key blocks add into this (b, h, i) in ascending order n = 0, 1, ...
-            ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(ticket) != w.n) {
-              if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
-                if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
-                st_shared(sh.abort(), 1);
-                stop = true;
-                break;
-              }
-              __nanosleep(64);
-            }
-            if (stop) break;
-          }
-          tma_reduce_add_3d(tdq, sh.dq_stage_addr(), 0, h, w.b * p.Sq + kBM * i + kDqRows * half);
-          bulk_commit_group();
-          if (p.deterministic && half == 1) {
-            bulk_wait_group0();              // both halves are added ...
-            __threadfence();
-            st_release_gpu(ticket, w.n + 1);  // ... before the next key block may add
-          } else {
-            bulk_wait_group_read0();         // the staging tile may be overwritten
-          }
-          mbar_arrive(sh.dqs_free());
-        }
+        mbar_arrive(sh.dqs_full(half));
       }
       if (stop) break;
     }
-    if (ld_shared_volatile(sh.abort())) break;
+    if (stop || ld_shared_volatile(sh.abort())) break;
     // epilogue of the unit: dV and scale * dK rows in BF16
     const int key = kBN * w.n + d;
     const bool valid = key < p.Sk;
@@ -580,7 +550,63 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const CUtensorMap
       ++ukv;
     }
   }
-  if (first) bulk_wait_group0();   // outstanding reductions finish before the CTA exits
+}
+
+// dQ reduce issuer (one thread): adds each staging tile into the FP32
+// accumulator with one TMA bulk tensor reduce-add.  Tile b of step t is freed
+// once the unit has read it, which is known when at most one later group is
+// still reading (the other tile), so one tile is always being written while
+// the other is read.  Out-of-range rows are skipped by the unit; rows of a
+// padded query block that belong to the next sequence receive exact zeros,
+// since their weights are 0.
+__device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
+  uint32_t sit = 0;
+  bool pending1 = false;   // tile 1 of the previous step is still being read
+  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    const Unit w = decode_unit(u, p);
+    for (int s = 0; s < w.steps; ++s, ++sit) {
+      const int h = w.hk * p.group + s / w.nq;
+      const int i = w.i0 + s % w.nq;
+      int* ticket = nullptr;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (!mbar_wait_bounded(sh.dqs_full(half), sit & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns))
+          goto done;
+        if (p.deterministic && half == 0) {
+          // key blocks add into this (b, h, i) in ascending order n = 0, 1, ...
+          ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(ticket) != w.n) {
+            if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
+              if (atomicCAS(&g_err.status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&g_err.site, kSiteDqTicket);
+              st_shared(sh.abort(), 1);
+              goto done;
+            }
+            __nanosleep(64);
+          }
+        }
+        tma_reduce_add_3d(tdq, sh.dq_stage_addr(half), 0, h, w.b * p.Sq + kBM * i + kDqRows * half);
+        bulk_commit_group();
+        bulk_wait_group_read1();   // every group but this one has been read
+        if (half == 0) {
+          if (pending1) mbar_arrive(sh.dqs_free(1));
+          pending1 = false;
+        } else {
+          mbar_arrive(sh.dqs_free(0));
+          pending1 = true;
+        }
+      }
+      if (p.deterministic) {
+        bulk_wait_group0();                // both tiles are added ...
+        __threadfence();
+        st_release_gpu(ticket, w.n + 1);   // ... before the next key block may add
+        mbar_arrive(sh.dqs_free(1));
+        pending1 = false;
+      }
+    }
+  }
+done:
+  bulk_wait_group0();   // outstanding reductions finish before the CTA exits
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -609,8 +635,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(sh.acc_full(), 1);
     mbar_init(sh.acc_empty(), 128);
-    mbar_init(sh.dqs_full(), 128);
-    mbar_init(sh.dqs_free(), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sh.dqs_full(b), 128);
+      mbar_init(sh.dqs_free(b), 1);
+    }
     st_shared(sh.abort(), 0);
     fence_barrier_init();
   }
@@ -633,11 +661,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     elementwise_role(sh, tmem, p, total_units);
   } else if (warp < 8) {
-    dq_role(sh, tmem, &tm_dqacc, p, total_units);
+    dq_role(sh, tmem, p, total_units);
   } else if (warp == 8) {
     if ((threadIdx.x % 32) == 0) producer_role(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
   } else if (warp == 9) {
     mma_role(sh, tmem, p, total_units);   // converged warp; one elected lane issues
+  } else if (warp == 10) {
+    if ((threadIdx.x % 32) == 0) reduce_role(sh, &tm_dqacc, p, total_units);
   }
   if (ld_shared_volatile(sh.abort())) {
     const uint64_t t0 = globaltimer_ns();
