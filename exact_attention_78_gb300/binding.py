@@ -52,10 +52,14 @@ def lib_path():
 
 
 def load_library(build_if_missing=False):
-    """Loads (optionally builds) the in-tree shared library; raises if absent."""
+    """Loads the in-tree shared library; raises if absent.  With
+    build_if_missing, (re)builds it first when it is absent or older than a
+    source file."""
     global _LIB
     if _LIB is not None:
         return _LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
     if not os.path.exists(_build.LIB):
         if not build_if_missing:
             raise RuntimeError("CUDA library %s is not built; run exact_attention_78_gb300.build.build()"
