@@ -48,6 +48,8 @@ def parse():
                     help="dense: B,H,S,D below; train: B=2 H=16 S=8192 D=128 causal; "
                          "varlen: 64 packed sequences, Hq=32 Hkv=8, D=128, causal (forward only)")
     ap.add_argument("--deterministic", action="store_true", help="deterministic dQ order in the backward")
+    ap.add_argument("--paired", action="store_true",
+                    help="backward main kernel on CTA pairs (paired tcgen05 MMAs) instead of single CTAs")
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--fwd-only", action="store_true", help="time the forward call alone")
     ap.add_argument("--B", type=int, default=4)
@@ -138,6 +140,7 @@ def measured_traffic(kernel, w):
         return None
     csrc = os.path.join(ROOT, "exact_attention_78_gb300", "csrc")
     files = {"bwd_kernel": ["fa_bwd.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"],
+             "bwd_pair_kernel": ["fa_bwd_pair.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"],
              "fwd_kernel": ["fa_fwd.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"]}[kernel]
     m = hashlib.sha256()
     for fn in files:
@@ -250,6 +253,7 @@ def run_gpu(args):
     lse = torch.empty(lse_shape, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     det = bool(w.extra.get("deterministic", args.deterministic))
+    paired = True if args.paired else None
 
     have_bwd = not args.fwd_only and not w.packed
     ws_buf = dq = dk = dv = None
@@ -260,7 +264,7 @@ def run_gpu(args):
             dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
             fa.fwd(qd, kd, vd, causal=w.causal, out=o, lse=lse, emu_per_16=args.emu)
             fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
-                   dv=dv)
+                   dv=dv, paired=paired)
         except fa.FAError as e:
             if e.status != 2:
                 raise
@@ -279,7 +283,7 @@ def run_gpu(args):
             ev_f1[i].record(stream)
         if have_bwd:
             fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
-                   dv=dv)
+                   dv=dv, paired=paired)
         if i is not None:
             ev_b1[i].record(stream)
 
@@ -359,10 +363,11 @@ def run_gpu(args):
         dom, dom_ms, dom_flops = "bwd", bwd_ms, 2.5 * fwd_flops_of(w)
     else:
         dom, dom_ms, dom_flops = "fwd", fwd_ms, fwd_flops_of(w)
+    kname = "bwd_pair_kernel" if (dom == "bwd" and args.paired) else dom + "_kernel"
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": measured_traffic(dom + "_kernel", w), "kernel": dom,
+                "frac": achieved / peak, "traffic": measured_traffic(kname, w), "kernel": kname,
                 "peak_kind": "%s, sustained bf16 (kernel timed inside a repeated step)" % pk_kind}
 
     cpu = None
@@ -374,6 +379,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w.describe(), "step": "fwd+bwd" if have_bwd else "fwd", "deterministic": det,
+                   "bwd_kernel": "paired CTAs" if args.paired else "single CTA",
                    "l2": "inputs larger than L2 (Q,K,V,O %d MiB each)" % (qd.numel() * 2 >> 20),
                    "parallelism": "replicas" if ws > 1 else "single"},
         "fwd_tflops": fwd_flops_of(w) / (fwd_ms * 1e-3) / 1e12,

@@ -27,6 +27,10 @@ class FwdTuning(ctypes.Structure):
     _fields_ = [("rescale_threshold", ctypes.c_float), ("emu_per_16", ctypes.c_int)]
 
 
+class BwdTuning(ctypes.Structure):
+    _fields_ = [("paired", ctypes.c_int)]
+
+
 _LIB = None
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 
@@ -38,6 +42,9 @@ _SIGNATURES = {
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _i,
                     _vp, _sz, _vp]),
+    "fa_bwd_default_tuning": (BwdTuning, []),
+    "fa_bwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _i,
+                       _vp, _sz, ctypes.POINTER(BwdTuning), _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
                             _i, _vp]),
     "fa_get_device_error": (_i, [_vp]),
@@ -145,8 +152,9 @@ def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic=False):
 
 
 def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, workspace=None, dq=None, dk=None,
-        dv=None, stream=None):
-    """dQ, dK, dV of attention(q, k, v) given O, LSE and dO (dense layout)."""
+        dv=None, paired=None, stream=None):
+    """dQ, dK, dV of attention(q, k, v) given O, LSE and dO (dense layout).
+    paired=True runs the main kernel on CTA pairs (paired tcgen05 MMAs)."""
     lib = load_library()
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check_bf16(n, t)
@@ -159,9 +167,15 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, work
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
-                    Hkv, Sq, Sk, D, int(bool(causal)), float(scale), None, int(bool(deterministic)),
-                    _ptr(workspace), workspace.numel(), _stream(stream))
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq,
+            Sk, D, int(bool(causal)), float(scale), None, int(bool(deterministic)), _ptr(workspace),
+            workspace.numel()]
+    if paired is None:
+        st = lib.fa_bwd(*args, _stream(stream))
+    else:
+        t = lib.fa_bwd_default_tuning()
+        t.paired = int(bool(paired))
+        st = lib.fa_bwd_ex(*args, ctypes.byref(t), _stream(stream))
     _check(st, "fa_bwd")
     return dq, dk, dv
 

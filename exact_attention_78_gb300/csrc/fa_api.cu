@@ -84,13 +84,13 @@ fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, i
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D,
+fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_d,
                                      int box_rows) {
   auto fn = encode_fn();
   if (!fn) return FA_ERR_CUDA;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)heads * D * 4};
-  const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows};
+  const cuuint32_t box[3] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -109,7 +109,7 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministi
   w.nlse2 = off;
   off = align256(off + (size_t)B * Hq * sq_pad * sizeof(float));
   w.tickets = off;
-  if (deterministic) off = align256(off + (size_t)B * Hq * (sq_pad / 64) * sizeof(int));
+  if (deterministic) off = align256(off + (size_t)B * Hq * (sq_pad / 64) * 2 * sizeof(int));
   w.total = off;
   return w;
 }
@@ -187,11 +187,22 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int 
   return bwd_workspace_layout(B, Hq, Sq, D, deterministic).total;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
-                 float scale, const int* cu_seqlens, int deterministic, void* workspace,
-                 size_t workspace_bytes, fa_stream_t stream) {
+fa_bwd_tuning fa_bwd_default_tuning(void) {
+  fa_bwd_tuning t;
+  t.paired = 0;
+  return t;
+}
+
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                    int causal, float scale, const int* cu_seqlens, int deterministic, void* workspace,
+                    size_t workspace_bytes, const fa_bwd_tuning* t, fa_stream_t stream) {
   try {
+    fa_bwd_tuning tune = fa_bwd_default_tuning();
+    if (t) {
+      if (t->paired < -1 || t->paired > 1) return FA_ERR_INVALID_ARG;
+      if (t->paired >= 0) tune.paired = t->paired;
+    }
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
     for (const void* p : ptrs)
@@ -236,16 +247,26 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     L.p.scale_log2 = scale * kLog2e;
     L.p.wait_limit_ns = kDefaultWaitLimitNs;
     L.num_sms = num_sms;
+    L.pair = tune.paired != 0;
     return launch_bwd(L, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {
     return FA_ERR_CUDA;
   }
 }
 
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk, int D, int causal,
+                 float scale, const int* cu_seqlens, int deterministic, void* workspace,
+                 size_t workspace_bytes, fa_stream_t stream) {
+  return fa_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, D, causal, scale, cu_seqlens,
+                   deterministic, workspace, workspace_bytes, nullptr, stream);
+}
+
 fa_status fa_get_device_error(fa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   fa_status first = FA_OK;
-  const fa_status all[3] = {fwd_take_device_error(), bwd_take_device_error(), diag_take_device_error()};
+  const fa_status all[4] = {fwd_take_device_error(), bwd_take_device_error(), bwd_pair_take_device_error(),
+                            diag_take_device_error()};
   for (fa_status s : all)
     if (first == FA_OK && s != FA_OK) first = s;
   return first;

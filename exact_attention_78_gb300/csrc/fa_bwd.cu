@@ -686,17 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   const BwdParams& p = L.p;
   if (p.D != bwd::kD) return FA_ERR_UNSUPPORTED;
-  CUtensorMap tq, tk, tv, tdo, tdq;
   fa_status st;
-  if ((st = make_tmap_f32_rows_heads_d(&tdq, p.dq_acc, p.B * p.Sq, p.Hq, p.D, bwd::kDqRows)) != FA_OK) return st;
-  if ((st = make_tmap_rows_heads_d(&tq, L.q, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
-  if ((st = make_tmap_rows_heads_d(&tdo, p.dout, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
-  if ((st = make_tmap_rows_heads_d(&tk, L.k, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
-  if ((st = make_tmap_rows_heads_d(&tv, L.v, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
 
   // pre: Delta, LSE2, zero accumulator and tickets
   const long long rows = (long long)p.B * p.Hq * p.sq_pad;
-  const long long n_tickets = p.deterministic ? (long long)p.B * p.Hq * p.nqb : 0;
+  const long long n_tickets = p.deterministic ? (long long)p.B * p.Hq * p.nqb * 2 : 0;
   long long pre_blocks = (rows * 32 + 255) / 256;
   if (pre_blocks > 16 * L.num_sms) pre_blocks = 16 * L.num_sms;
   if (pre_blocks < 1) pre_blocks = 1;
@@ -705,17 +699,28 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
       p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.B, p.Hq, p.Sq, p.sq_pad);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(bwd::bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bwd::Layout::kDynamic) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_done = true;
+  if (L.pair) {
+    if ((st = launch_bwd_pair_main(L, stream)) != FA_OK) return st;
+  } else {
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    if ((st = make_tmap_f32_rows_heads_d(&tdq, p.dq_acc, p.B * p.Sq, p.Hq, p.D, p.D, bwd::kDqRows)) != FA_OK)
+      return st;
+    if ((st = make_tmap_rows_heads_d(&tq, L.q, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
+    if ((st = make_tmap_rows_heads_d(&tdo, p.dout, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
+    if ((st = make_tmap_rows_heads_d(&tk, L.k, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
+    if ((st = make_tmap_rows_heads_d(&tv, L.v, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
+    static bool attr_done = false;
+    if (!attr_done) {
+      if (cudaFuncSetAttribute(bwd::bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bwd::Layout::kDynamic) != cudaSuccess)
+        return FA_ERR_CUDA;
+      attr_done = true;
+    }
+    const long long units = (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
+    const int grid = (int)(units < L.num_sms ? units : L.num_sms);
+    bwd::bwd_kernel<<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
-  const long long units = (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
-  const int grid = (int)(units < L.num_sms ? units : L.num_sms);
-  bwd::bwd_kernel<<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
   // post: dQ = BF16(scale * accumulator)
   const long long n8 = (long long)p.B * p.Sq * p.Hq * p.D / 8;

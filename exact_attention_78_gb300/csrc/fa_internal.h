@@ -48,7 +48,7 @@ struct BwdParams {
   float* dq_acc;     // [B, Sq, Hq, D] fp32
   float* ndelta;     // [B, Hq, sq_pad]  -sum_d dO * O
   float* nlse2;      // [B, Hq, sq_pad]  -lse * log2(e)
-  int* tickets;      // [B, Hq, nqb] or nullptr
+  int* tickets;      // [B, Hq, nqb, 2] or nullptr
   int B, Hq, Hkv, Sq, Sk, D;
   int sq_pad;        // Sq rounded up to a multiple of 64
   int nqb;           // 64-row query blocks: sq_pad / 64
@@ -66,6 +66,7 @@ struct BwdLaunch {
   const void* v;
   BwdParams p;
   int num_sms;
+  bool pair;   // main kernel on CTA pairs (paired MMAs) rather than single CTAs
 };
 
 // Workspace carve-up of the backward pass (all offsets 256-byte aligned).
@@ -77,14 +78,15 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministi
 // 3-D tiled tensor map over a [rows, heads, D] BF16 array (D contiguous) with
 // a box of 64 x 1 x box_rows and 128-byte swizzle.
 fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_rows);
-// Same view over an FP32 [rows, heads, D] array, box D x 1 x box_rows, no
+// Same view over an FP32 [rows, heads, D] array, box box_d x 1 x box_rows, no
 // swizzle (a row-major staging tile).
-fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D,
+fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_d,
                                      int box_rows);
 
 // Kernel launchers (defined in their translation units).
 fa_status launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+fa_status launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream);
 fa_status launch_diag_exp2(const float* x, float* y_emu, float* y_hw, long long n, cudaStream_t stream);
 fa_status launch_diag_wait(unsigned long long limit_ns, cudaStream_t stream);
 
@@ -92,6 +94,7 @@ fa_status launch_diag_wait(unsigned long long limit_ns, cudaStream_t stream);
 // clear it (returning FA_OK when clean).
 fa_status fwd_take_device_error();
 fa_status bwd_take_device_error();
+fa_status bwd_pair_take_device_error();
 fa_status diag_take_device_error();
 
 // Shared-memory alignment slack added to every dynamic allocation.

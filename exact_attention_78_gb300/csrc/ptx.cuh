@@ -95,6 +95,86 @@ FA_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t abort, Dev
   }
 }
 
+// ---------------------------------------------------------------- cluster --
+
+FA_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+FA_DEV uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+FA_DEV uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the object at local shared address `addr` in the
+// CTA of cluster rank `rank`.
+FA_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+FA_DEV void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+FA_DEV void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+// Orders this thread's generic-proxy writes to shared memory of any CTA of
+// the cluster before later async-proxy (tensor core, TMA) reads.
+FA_DEV void fence_proxy_async_cluster() { asm volatile("fence.proxy.async.shared::cluster;" ::: "memory"); }
+// Arrive on a barrier given by its shared::cluster address (possibly in the
+// other CTA of the pair); release at cluster scope orders this thread's
+// earlier memory operations before the arrival.
+FA_DEV void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Same without memory ordering: for hand-offs that only order tcgen05
+// operations (a TMEM read before the producer may overwrite it), which
+// tcgen05.wait plus tcgen05.fence::before_thread_sync already order.
+FA_DEV void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+FA_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire, for barriers that the other CTA of
+// the pair arrives on.  Same give-up rules as mbar_wait_bounded.
+FA_DEV bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity, uint32_t abort, DeviceError* err, int site,
+                                      uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (ld_shared_volatile(abort)) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        if (err && atomicCAS(&err->status, 0, FA_ERR_TIMEOUT) == 0) atomicExch(&err->site, site);
+        st_shared(abort, 1);
+        return false;
+      }
+    }
+  }
+}
+// All threads of both CTAs of the cluster (warps converged).
+FA_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA --
 
 // 3-D tiled bulk tensor load into shared memory, completing on `bar`.
@@ -266,6 +346,76 @@ FA_DEV uint32_t desc_hi(uint64_t d) { return static_cast<uint32_t>(d >> 32); }
 FA_DEV void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+// ---------------------------------------------------- CTA-pair tcgen05 --
+// Paired (cta_group::2) forms.  TMEM is allocated collectively by one warp of
+// each CTA of the pair (both receive the same address).  One thread of the
+// even CTA issues the MMAs: with M = 256 the CTA of rank r supplies rows
+// [128 r, 128 r + 128) of A from its own shared memory (or TMEM) and receives
+// the same rows of D in its TMEM lanes 0-127; B is split along N, the CTA of
+// rank r supplying columns [r N/2, (r+1) N/2) from the first N/2 rows (K-major)
+// or elements (MN-major) at the descriptor address in its own shared memory.
+// With M = 128 each CTA supplies 64 rows of A, and its D (64 rows x N) lands
+// folded in its TMEM as lane 64 j + row, column c <-> (row, N/2 j + c).
+
+FA_DEV void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+FA_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+FA_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+template <uint32_t AOFF, uint32_t BOFF>
+FA_DEV void mma_pair_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "add.u32 al, %1, %7;\n\t"
+      "add.u32 bl, %3, %8;\n\t"
+      "mov.b64 ad, {al, %2};\n\t"
+      "mov.b64 bd, {bl, %4};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %5, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+      : "memory");
+}
+template <uint32_t AOFF, uint32_t BOFF>
+FA_DEV void mma_pair_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t.reg .b32 at, bl;\n\t.reg .b64 bd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 at, %1, %6;\n\t"
+      "add.u32 bl, %2, %7;\n\t"
+      "mov.b64 bd, {bl, %3};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], bd, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+      : "memory");
+}
+// Arrives once on the barrier at local shared address `bar` in both CTAs of
+// the pair when every paired tcgen05 operation issued so far has completed.
+FA_DEV void mma_pair_commit_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}\n" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// Shared-memory matrix descriptor for a 64-byte-swizzled MN-major operand:
+// 64 B (32 BF16) along M/N per row, one row per K index, 8-row groups `sbo`
+// bytes apart, in 512-byte-aligned swizzle atoms.
+FA_DEV uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46)  // descriptor version for tcgen05
+         | (4ull << 61);                                           // 64-byte swizzle
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives lane

@@ -94,7 +94,7 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
  * The workspace holds the FP32 dQ accumulator [B, Sq, Hq, D], the per-row
  * terms -Delta_i = -sum_d dO_id * O_id and -LSE * log2(e) (FP32
  * [B, Hq, Sq rounded up to a multiple of 64] each) and, when `deterministic`
- * is set, one int32 ticket per (b, h, 64-row query block).  Returns 0 for
+ * is set, two int32 tickets per (b, h, 64-row query block).  Returns 0 for
  * arguments fa_bwd() would reject (including D != 128).
  */
 FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic);

@@ -42,6 +42,36 @@ FA_API fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o,
                            const fa_fwd_tuning* t, fa_stream_t stream);
 
 /*
+ * Backward-pass knobs (fa_bwd uses the defaults).
+ *   paired  1: the main kernel runs on two-CTA clusters and issues every
+ *           product as a paired (cta_group::2) tcgen05 MMA over two adjacent
+ *           key blocks ("FlashAttention-4: Algorithm and Kernel Pipelining
+ *           Co-Design ...", bullet "Paired-CTA backward pass"): each CTA
+ *           reads only half of every B operand from shared memory and the
+ *           pair adds each dQ element once instead of twice.  0: one CTA per
+ *           key block, every product on one SM.  Negative selects the
+ *           default, 0: on GB300 the unpaired kernel is faster, because the
+ *           paired dQ product needs the two CTAs to exchange dS^T through
+ *           distributed shared memory (thousands of cycles of latency that
+ *           the fully used tensor memory leaves no room to hide) and runs
+ *           at 64 rows per SM.
+ */
+typedef struct {
+  int paired;
+} fa_bwd_tuning;
+
+/* The defaults fa_bwd() uses. */
+FA_API fa_bwd_tuning fa_bwd_default_tuning(void);
+
+/* fa_bwd() with explicit knobs; `t` may be NULL for the defaults.  Same
+ * arguments, workspace and errors as fa_bwd(); FA_ERR_INVALID_ARG if
+ * t->paired is not -1, 0 or 1. */
+FA_API fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk,
+                           int D, int causal, float scale, const int* cu_seqlens, int deterministic,
+                           void* workspace, size_t workspace_bytes, const fa_bwd_tuning* t, fa_stream_t stream);
+
+/*
  * Evaluates 2^x for n FP32 inputs both ways the softmax can: y_emu with the
  * FMA-unit polynomial (split x into floor and fraction, cubic on the
  * fraction, add the integer to the exponent bits), y_hw with the hardware

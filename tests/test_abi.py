@@ -82,7 +82,7 @@ def test_workspace_size(lib):
     rows = 2 * 16 * 8192 * 4
     assert n == acc + 2 * rows
     det = lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 1)
-    assert det == n + 2 * 16 * 128 * 4          # one ticket per 64-row query block
+    assert det == n + 2 * 16 * 128 * 2 * 4      # two tickets (feature halves) per 64-row query block
     # ragged rows: the per-row terms are padded to a multiple of 64 rows
     r = lib.fa_bwd_workspace_size(1, 2, 2, 100, 100, 128, 0)
     assert r == (1 * 100 * 2 * 128 * 4 + 255) // 256 * 256 + 2 * (1 * 2 * 128 * 4)
@@ -104,6 +104,15 @@ def test_backward_rejects_bad_arguments(lib):
     assert call(ws=None) == 5
     assert call(ws=ctypes.c_void_p(A.value + 16)) == 5
     assert call(ws_bytes=100) == 5
+
+
+def test_backward_tuning_validation(lib):
+    from exact_attention_78_gb300.binding import BwdTuning
+    assert lib.fa_bwd_default_tuning().paired == 0
+    for paired in (2, -2, 7):
+        bad = BwdTuning(paired)
+        assert lib.fa_bwd_ex(A, A, A, A, A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, 0.125, None, 0, A, 1 << 40,
+                             ctypes.byref(bad), None) == 1
 
 
 def test_diag_argument_checks(lib):
