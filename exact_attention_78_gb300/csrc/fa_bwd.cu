@@ -559,9 +559,24 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
 // the other is read.  Out-of-range rows are skipped by the unit; rows of a
 // padded query block that belong to the next sequence receive exact zeros,
 // since their weights are 0.
+//
+// Deterministic mode: key blocks add into each (b, h, i) in ascending order
+// n = 0, 1, ..., one ticket per (b, h, i) holding the next block allowed to
+// add.  A step's ticket is released one step late, once the next step's two
+// reductions are issued and at most those two are still pending, so the
+// completion latency of the additions is not paid per step.  Waits point
+// only from key block n to block n - 1 of the same head, and no ticket is
+// held across units (heads), so the waits cannot form a cycle.
 __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
   uint32_t sit = 0;
   bool pending1 = false;   // tile 1 of the previous step is still being read
+  int* held = nullptr;     // deterministic mode: ticket of the previous step, not yet released
+  int held_next = 0;
+  auto release_held = [&]() {
+    __threadfence();
+    st_release_gpu(held, held_next);
+    held = nullptr;
+  };
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit(u, p);
     for (int s = 0; s < w.steps; ++s, ++sit) {
@@ -573,7 +588,6 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
         if (!mbar_wait_bounded(sh.dqs_full(half), sit & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns))
           goto done;
         if (p.deterministic && half == 0) {
-          // key blocks add into this (b, h, i) in ascending order n = 0, 1, ...
           ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
           const uint64_t t0 = globaltimer_ns();
           while (ld_acquire_gpu(ticket) != w.n) {
@@ -597,16 +611,23 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
         }
       }
       if (p.deterministic) {
-        bulk_wait_group0();                // both tiles are added ...
-        __threadfence();
-        st_release_gpu(ticket, w.n + 1);   // ... before the next key block may add
-        mbar_arrive(sh.dqs_free(1));
-        pending1 = false;
+        if (held) {
+          bulk_wait_group2();   // the previous step's two additions are complete
+          release_held();
+        }
+        held = ticket;
+        held_next = w.n + 1;
       }
+    }
+    if (held) {
+      // end of the unit: no ticket is held while waiting on another head's
+      bulk_wait_group0();
+      release_held();
     }
   }
 done:
   bulk_wait_group0();   // outstanding reductions finish before the CTA exits
+  if (held) release_held();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)

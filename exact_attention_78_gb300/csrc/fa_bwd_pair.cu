@@ -547,10 +547,20 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
 // with TMA bulk tensor reduce-adds.  Out-of-range rows are skipped by the
 // unit; rows of a padded query block that belong to the next sequence receive
 // exact zeros, since their weights are 0.  Deterministic mode: the pairs add
-// into one (b, h, i, feature half) in ascending pair order m = 0, 1, ...
+// into one (b, h, i, feature half) in ascending pair order m = 0, 1, ...; a
+// step's ticket is released one step late (once at most the next step's two
+// additions are pending), and never held across units, so waits point only
+// from pair m to pair m - 1 of the same head.
 __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
   const int r = (int)sh.rank;
   uint32_t sit = 0;
+  int* held = nullptr;
+  int held_next = 0;
+  auto release_held = [&]() {
+    __threadfence();
+    st_release_gpu(held, held_next);
+    held = nullptr;
+  };
   for (int u = cluster_id_x(); u < total_units; u += nclusters_x()) {
     const Unit w = decode_unit(u, p, r);
     for (int s = 0; s < w.steps; ++s, ++sit) {
@@ -571,21 +581,29 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
         }
       }
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
+      for (int j = 0; j < 2; ++j) {
         tma_reduce_add_3d(tdq, sh.dq_stage_addr(j), 64 * r, h, w.b * p.Sq + kBM * i + kHalf * j);
-      bulk_commit_group();
-      if (p.deterministic) {
-        bulk_wait_group0();                // both tiles are added ...
-        __threadfence();
-        st_release_gpu(ticket, w.m + 1);   // ... before the next pair may add
-      } else {
-        bulk_wait_group_read0();           // the staging tiles may be overwritten
+        bulk_commit_group();
       }
+      bulk_wait_group_read0();   // the staging tiles may be overwritten
       mbar_arrive(sh.dqs_free());
+      if (p.deterministic) {
+        if (held) {
+          bulk_wait_group2();    // the previous step's two additions are complete
+          release_held();
+        }
+        held = ticket;
+        held_next = w.m + 1;
+      }
+    }
+    if (held) {
+      bulk_wait_group0();
+      release_held();
     }
   }
 done:
   bulk_wait_group0();   // outstanding reductions finish before the CTA exits
+  if (held) release_held();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_pair_kernel(const __grid_constant__ Maps mp, const BwdParams p) {
