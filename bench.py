@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="dense", choices=["dense", "train", "varlen"],
                     help="dense: B,H,S,D below; train: B=2 H=16 S=8192 D=128 causal; "
-                         "varlen: 64 packed sequences, Hq=32 Hkv=8, D=128, causal (forward only)")
+                         "varlen: 64 packed sequences, Hq=32 Hkv=8, D=128, causal")
     ap.add_argument("--deterministic", action="store_true", help="deterministic dQ order in the backward")
     ap.add_argument("--paired", action="store_true",
                     help="backward main kernel on CTA pairs (paired tcgen05 MMAs) instead of single CTAs")
@@ -255,16 +255,20 @@ def run_gpu(args):
     det = bool(w.extra.get("deterministic", args.deterministic))
     paired = True if args.paired else None
 
-    have_bwd = not args.fwd_only and not w.packed
+    have_bwd = not args.fwd_only
     ws_buf = dq = dk = dv = None
     if have_bwd:
         try:
-            need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, det)
+            if w.packed:
+                rows = qd.shape[0]
+                need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, rows, rows, w.D, det, total_q=rows)
+            else:
+                need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, det)
             ws_buf = torch.empty(need, dtype=torch.uint8, device="cuda")
             dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-            fa.fwd(qd, kd, vd, causal=w.causal, out=o, lse=lse, emu_per_16=args.emu)
+            fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, emu_per_16=args.emu)
             fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
-                   dv=dv, paired=paired)
+                   dv=dv, paired=paired, cu_seqlens=cud)
         except fa.FAError as e:
             if e.status != 2:
                 raise
@@ -283,7 +287,7 @@ def run_gpu(args):
             ev_f1[i].record(stream)
         if have_bwd:
             fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
-                   dv=dv, paired=paired)
+                   dv=dv, paired=paired, cu_seqlens=cud)
         if i is not None:
             ev_b1[i].record(stream)
 

@@ -39,7 +39,7 @@ _SIGNATURES = {
     "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
                        ctypes.POINTER(FwdTuning), _vp]),
     "fa_fwd_default_tuning": (FwdTuning, []),
-    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int), _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _i,
                     _vp, _sz, _vp]),
     "fa_bwd_default_tuning": (BwdTuning, []),
@@ -147,28 +147,36 @@ def fwd(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, 
     return out, lse
 
 
-def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic=False):
-    return int(load_library().fa_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, int(bool(deterministic))))
+def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic=False, total_q=0, cu_seqlens_host=None):
+    """Workspace bytes of fa_bwd.  Packed layout: total_q = packed row count
+    (= Sq = Sk); cu_seqlens_host, if given, is a host sequence of B + 1 offsets."""
+    offs = None
+    if cu_seqlens_host is not None:
+        vals = [int(x) for x in cu_seqlens_host]
+        offs = (ctypes.c_int * len(vals))(*vals)
+    return int(load_library().fa_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, offs, int(total_q),
+                                                    int(bool(deterministic))))
 
 
 def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, workspace=None, dq=None, dk=None,
-        dv=None, paired=None, stream=None):
-    """dQ, dK, dV of attention(q, k, v) given O, LSE and dO (dense layout).
-    paired=True runs the main kernel on CTA pairs (paired tcgen05 MMAs)."""
+        dv=None, paired=None, cu_seqlens=None, stream=None):
+    """dQ, dK, dV of attention(q, k, v) given O, LSE and dO.  Dense [B,S,H,D]
+    or packed [total,H,D] with cu_seqlens (LSE [Hq, total]).  paired=True runs
+    the main kernel on CTA pairs (paired tcgen05 MMAs; dense only)."""
     lib = load_library()
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check_bf16(n, t)
-    B, Hq, Hkv, Sq, Sk, D = _dims(q, k, None)
+    B, Hq, Hkv, Sq, Sk, D = _dims(q, k, cu_seqlens)
     if scale is None:
         scale = D ** -0.5
-    need = bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic)
+    need = bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic, total_q=Sq if cu_seqlens is not None else 0)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq,
-            Sk, D, int(bool(causal)), float(scale), None, int(bool(deterministic)), _ptr(workspace),
+            Sk, D, int(bool(causal)), float(scale), _ptr(cu_seqlens), int(bool(deterministic)), _ptr(workspace),
             workspace.numel()]
     if paired is None:
         st = lib.fa_bwd(*args, _stream(stream))

@@ -98,19 +98,26 @@ fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int row
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic) {
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic, bool packed) {
   BwdWorkspace w{};
-  const size_t sq_pad = (size_t(Sq) + 63) / 64 * 64;
+  // row terms per head: dense, Sq rounded up to 64 per batch entry; packed,
+  // every sequence rounded up to 64 rows, bounded by total + 64 per sequence
+  const size_t sq_pad = packed ? (size_t(Sq) + 63) / 64 * 64 + 64 * size_t(B) : (size_t(Sq) + 63) / 64 * 64;
+  const size_t rows = packed ? size_t(Sq) : size_t(B) * Sq;       // rows of the accumulator
+  const size_t heads_rt = packed ? size_t(Hq) : size_t(B) * Hq;  // row-term arrays of sq_pad floats
   size_t off = 0;
   w.dq_acc = off;
-  off = align256(off + (size_t)B * Sq * Hq * D * sizeof(float));
+  off = align256(off + rows * Hq * D * sizeof(float));
   w.ndelta = off;
-  off = align256(off + (size_t)B * Hq * sq_pad * sizeof(float));
+  off = align256(off + heads_rt * sq_pad * sizeof(float));
   w.nlse2 = off;
-  off = align256(off + (size_t)B * Hq * sq_pad * sizeof(float));
+  off = align256(off + heads_rt * sq_pad * sizeof(float));
+  w.plan = off;
+  if (packed) off = align256(off + (2 * size_t(B) + 4) * sizeof(int));
   w.tickets = off;
-  if (deterministic) off = align256(off + (size_t)B * Hq * (sq_pad / 64) * 2 * sizeof(int));
+  if (deterministic) off = align256(off + heads_rt * (sq_pad / 64) * 2 * sizeof(int));
   w.total = off;
+  w.sq_pad = (int)sq_pad;
   return w;
 }
 
@@ -180,11 +187,27 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   return fa_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, causal, scale, cu_seqlens, nullptr, stream);
 }
 
-size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic) {
-  if (check_shapes(B, Hq, Hkv, Sq, Sk, D, 1.0f, nullptr) != FA_OK) return 0;
+size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, const int* cu_seqlens_host,
+                             int total_q, int deterministic) {
   if (deterministic != 0 && deterministic != 1) return 0;
-  if (D != 128) return 0;
-  return bwd_workspace_layout(B, Hq, Sq, D, deterministic).total;
+  if (D != 128 || total_q < 0) return 0;
+  const bool packed = cu_seqlens_host != nullptr || total_q > 0;
+  if (!packed) {
+    if (check_shapes(B, Hq, Hkv, Sq, Sk, D, 1.0f, nullptr) != FA_OK) return 0;
+    return bwd_workspace_layout(B, Hq, Sq, D, deterministic, false).total;
+  }
+  // packed: Sq = Sk = total_q rows (any 4-aligned non-null marker passes the
+  // pointer checks of check_shapes; the offsets themselves are checked below)
+  static const int kMarker[1] = {0};
+  if (Sq != total_q || Sk != total_q) return 0;
+  if (check_shapes(B, Hq, Hkv, Sq, Sk, D, 1.0f, kMarker) != FA_OK) return 0;
+  if (cu_seqlens_host) {
+    if (cu_seqlens_host[0] != 0 || cu_seqlens_host[B] != total_q) return 0;
+    for (int b = 0; b < B; ++b)
+      if (cu_seqlens_host[b + 1] < cu_seqlens_host[b] || cu_seqlens_host[b + 1] - cu_seqlens_host[b] > 262144)
+        return 0;
+  }
+  return bwd_workspace_layout(B, Hq, Sq, D, deterministic, true).total;
 }
 
 fa_bwd_tuning fa_bwd_default_tuning(void) {
@@ -211,8 +234,10 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
     fa_status st = check_shapes(B, Hq, Hkv, Sq, Sk, D, scale, cu_seqlens);
     if (st != FA_OK) return st;
-    if (cu_seqlens != nullptr || D != 128) return FA_ERR_UNSUPPORTED;
-    const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Sq, D, deterministic);
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+    const bool packed = cu_seqlens != nullptr;
+    if (packed && tune.paired == 1) return FA_ERR_UNSUPPORTED;   // the paired kernel is dense only
+    const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Sq, D, deterministic, packed);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < ws.total)
       return FA_ERR_WORKSPACE;
     int num_sms = 0;
@@ -231,9 +256,11 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.dq_acc = reinterpret_cast<float*>(wb + ws.dq_acc);
     L.p.ndelta = reinterpret_cast<float*>(wb + ws.ndelta);
     L.p.nlse2 = reinterpret_cast<float*>(wb + ws.nlse2);
-    L.p.sq_pad = (Sq + 63) / 64 * 64;
-    L.p.nqb = L.p.sq_pad / 64;
+    L.p.sq_pad = ws.sq_pad;
+    L.p.nqb = ws.sq_pad / 64;
     L.p.tickets = deterministic ? reinterpret_cast<int*>(wb + ws.tickets) : nullptr;
+    L.p.cu_seqlens = cu_seqlens;
+    L.p.plan = packed ? reinterpret_cast<int*>(wb + ws.plan) : nullptr;
     L.p.B = B;
     L.p.Hq = Hq;
     L.p.Hkv = Hkv;
@@ -247,7 +274,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.scale_log2 = scale * kLog2e;
     L.p.wait_limit_ns = kDefaultWaitLimitNs;
     L.num_sms = num_sms;
-    L.pair = tune.paired != 0;
+    L.pair = tune.paired == 1 && !packed;
     return launch_bwd(L, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {
     return FA_ERR_CUDA;

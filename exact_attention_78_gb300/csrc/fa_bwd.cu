@@ -140,9 +140,12 @@ __global__ void pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloa
   for (long long t = tid; t < n_tickets; t += (long long)gridDim.x * blockDim.x) tickets[t] = 0;
 }
 
-// dQ = BF16(scale * accumulator), eight elements per thread.
+// dQ = BF16(scale * accumulator), eight elements per thread.  Packed layout:
+// nothing is written when the plan kernel rejected the offsets (`rejected`
+// points at its status word; nullptr for the dense layout).
 __global__ void post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, long long n8,
-                            float scale) {
+                            float scale, const int* __restrict__ rejected) {
+  if (rejected && *rejected) return;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
@@ -156,45 +159,203 @@ __global__ void post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __r
   }
 }
 
+// ------------------------------------------------------------ packed layout --
+
+// One block of 1024 threads (B <= 1024 sequences): checks the offsets
+// (cu_seqlens[0] = 0, non-decreasing, at most 262,144 tokens per sequence,
+// cu_seqlens[B] = total) and writes the per-sequence tables of the packed
+// backward: plan[0..B] = prefix sums of 128-key blocks, plan[B+1..2B+1] =
+// prefix sums of the sequences' rows rounded up to 64 (where their row terms
+// and tickets start), plan[2B+2] = the total number of key blocks (0 when
+// the offsets are invalid, so that nothing is computed) and plan[2B+3] = 1
+// for invalid offsets, which is also reported as FA_ERR_INVALID_ARG.
+__global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ cu, int B, int total,
+                                                    int* __restrict__ plan) {
+  __shared__ int s_blk[1024], s_pad[1024];
+  __shared__ int bad;
+  const int t = threadIdx.x;
+  if (t == 0) bad = 0;
+  __syncthreads();
+  int nb = 0, np = 0;
+  if (t < B) {
+    const int a = cu[t], c = cu[t + 1];
+    const int len = c - a;
+    if (len < 0 || len > kMaxPairsPerSeq * 256 || (t == 0 && a != 0) || (t == B - 1 && c != total))
+      atomicOr(&bad, 1);
+    const int l = len < 0 ? 0 : len;
+    nb = (l + kBN - 1) / kBN;
+    np = (l + kBM - 1) / kBM * kBM;
+  }
+  s_blk[t] = nb;
+  s_pad[t] = np;
+  __syncthreads();
+  // inclusive prefix sums over the 1024 entries
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int x = t >= off ? s_blk[t - off] : 0;
+    const int y = t >= off ? s_pad[t - off] : 0;
+    __syncthreads();
+    s_blk[t] += x;
+    s_pad[t] += y;
+    __syncthreads();
+  }
+  if (t < B) {
+    plan[t] = t ? s_blk[t - 1] : 0;
+    plan[B + 1 + t] = t ? s_pad[t - 1] : 0;
+  }
+  if (t == 0) {
+    plan[B] = s_blk[B - 1];
+    plan[2 * B + 1] = s_pad[B - 1];
+    plan[2 * B + 2] = bad ? 0 : s_blk[B - 1];
+    plan[2 * B + 3] = bad;
+    if (bad && atomicCAS(&g_err.status, 0, FA_ERR_INVALID_ARG) == 0) atomicExch(&g_err.site, 0);
+  }
+}
+
+// Packed counterpart of pre_kernel.  Row terms live per head over the padded
+// rows of all sequences (sequence b from plan[B+1+b], rounded up to 64 rows);
+// padding rows get -inf and 0 so their weights are exactly 0.  One warp per
+// padded row; the real rows' dQ accumulator rows are zeroed.
+__global__ void pre_packed_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                                  const float* __restrict__ lse, const int* __restrict__ cu,
+                                  const int* __restrict__ plan, float* __restrict__ ndelta,
+                                  float* __restrict__ nlse2, float* __restrict__ dq_acc, int* __restrict__ tickets,
+                                  long long n_tickets, int B, int Hq, int total, int sq_pad) {
+  if (plan[2 * B + 3] != 0) return;   // offsets rejected: nothing is computed
+  const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)Hq * sq_pad;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int* pad = plan + B + 1;
+  for (long long r = warp_id; r < rows; r += nwarps) {
+    const int h = (int)(r / sq_pad);
+    const int pr = (int)(r % sq_pad);
+    float dl = 0.0f, l2 = -INFINITY;
+    if (pr < pad[B]) {
+      int lo = 0, hi = B;   // pad[lo] <= pr < pad[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pad[mid] <= pr) lo = mid;
+        else hi = mid;
+      }
+      const int off = pr - pad[lo];
+      if (off < cu[lo + 1] - cu[lo]) {
+        const int tok = cu[lo] + off;
+        const size_t e = ((size_t)tok * Hq + h) * kD + lane * 4;
+        const uint2 ov = *reinterpret_cast<const uint2*>(o + e);
+        const uint2 gv = *reinterpret_cast<const uint2*>(dout + e);
+        const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float2 a = __bfloat1622float2(op[k]), g = __bfloat1622float2(gp[k]);
+          acc = fmaf(a.x, g.x, acc);
+          acc = fmaf(a.y, g.y, acc);
+        }
+#pragma unroll
+        for (int sft = 16; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+        dl = -acc;
+        const float lv = lse[(size_t)h * total + tok];
+        l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
+        *reinterpret_cast<float4*>(dq_acc + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (lane == 0) {
+      ndelta[r] = dl;
+      nlse2[r] = l2;
+    }
+  }
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (long long t = tid; t < n_tickets; t += (long long)gridDim.x * blockDim.x) tickets[t] = 0;
+}
+
 // ------------------------------------------------------------ main kernel --
 
-// One work unit: key block n (128 keys) of one (batch, key/value head); its
-// steps run over the query heads of the group and the 64-row query blocks
-// that see at least one of its keys.
+// One work unit: key block n (128 keys) of one (batch entry or packed
+// sequence b, key/value head); its steps run over the query heads of the
+// group and the 64-row query blocks that see at least one of its keys.
 struct Unit {
   int b, hk, n;
-  int i0;      // first query block
-  int nq;      // query blocks per head (nqb - i0)
-  int steps;   // group * nq
+  int i0;           // first query block
+  int nq;           // query blocks per head (of the sequence, from i0)
+  int steps;        // group * nq
+  int qbase, kbase; // row of the sequence's first query / key in the [rows, H, D] arrays
+  int lq, lk;       // query / key count of the sequence
+  long long rt;     // row-term index of the sequence's first row for head 0 (+ h * sq_pad per head)
+  long long tk;     // ticket index of its first query block for head 0 (+ h * nqb per head)
 };
 
+// Work units of the call.  Packed layout: the plan kernel has stored the
+// number of 128-key blocks over all sequences (0 if the offsets are invalid).
+template <bool PACKED>
+__device__ __forceinline__ int total_units_of(const BwdParams& p) {
+  if constexpr (PACKED) return p.plan[2 * p.B + 2] * p.Hkv;
+  else return ((p.Sk + kBN - 1) / kBN) * p.B * p.Hkv;
+}
+
+// Per-sequence geometry of a unit.  The dense instantiation derives it from
+// the call's parameters instead of carrying it in registers.
+template <bool PACKED> FA_DEV int u_qbase(const Unit& w, const BwdParams& p) { return PACKED ? w.qbase : w.b * p.Sq; }
+template <bool PACKED> FA_DEV int u_kbase(const Unit& w, const BwdParams& p) { return PACKED ? w.kbase : w.b * p.Sk; }
+template <bool PACKED> FA_DEV int u_lq(const Unit& w, const BwdParams& p) { return PACKED ? w.lq : p.Sq; }
+template <bool PACKED> FA_DEV int u_lk(const Unit& w, const BwdParams& p) { return PACKED ? w.lk : p.Sk; }
+template <bool PACKED> FA_DEV size_t u_rt(const Unit& w, const BwdParams& p) {
+  return PACKED ? size_t(w.rt) : size_t(w.b) * p.Hq * p.sq_pad;
+}
+template <bool PACKED> FA_DEV size_t u_tk(const Unit& w, const BwdParams& p) {
+  return PACKED ? size_t(w.tk) : size_t(w.b) * p.Hq * p.nqb;
+}
+
+template <bool PACKED>
 __device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p) {
   Unit w;
-  // Head-major: the key blocks of one (batch, kv head) are adjacent, so the
-  // CTAs working at the same time share that head's Q / dO reads and its
-  // slice of the dQ accumulator in L2.  Within a head, key blocks come in
-  // ascending order: under a causal mask the early blocks see the most query
-  // rows, so each head's longest units come first.
-  const int nkv = (p.Sk + kBN - 1) / kBN;
-  int bh;
-  if (p.deterministic) {
-    // Deterministic mode orders each (b, h, query block)'s dQ additions by key
-    // block; key-block-major units put a block's predecessor in an earlier
-    // wave of the grid, so the ordered additions rarely wait.
-    bh = u % (p.B * p.Hkv);
-    w.n = u / (p.B * p.Hkv);
+  if constexpr (PACKED) {
+    // kv-head-major over the key blocks of all sequences in order: a
+    // sequence's blocks run together, and (deterministic mode) block n - 1
+    // of a sequence always has the smaller unit index
+    const int nb = p.plan[2 * p.B + 2];
+    w.hk = u / nb;
+    const int g = u % nb;
+    int lo = 0, hi = p.B;   // key-block prefix: plan[lo] <= g < plan[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.plan[mid] <= g) lo = mid;
+      else hi = mid;
+    }
+    w.b = lo;
+    w.n = g - p.plan[lo];
+    w.qbase = w.kbase = p.cu_seqlens[lo];
+    w.lq = w.lk = p.cu_seqlens[lo + 1] - w.qbase;
+    w.rt = p.plan[p.B + 1 + lo];   // padded-row prefix (multiple of 64)
+    w.tk = w.rt / kBM;
   } else {
-    bh = u / nkv;
-    w.n = u % nkv;
+    // Head-major: the key blocks of one (batch, kv head) are adjacent, so
+    // the CTAs working at the same time share that head's Q / dO reads and
+    // its slice of the dQ accumulator in L2.  Within a head, key blocks
+    // come in ascending order: under a causal mask the early blocks see the
+    // most query rows, so each head's longest units come first.
+    const int nkv = (p.Sk + kBN - 1) / kBN;
+    int bh;
+    if (p.deterministic) {
+      // Deterministic mode orders each (b, h, query block)'s dQ additions by
+      // key block; key-block-major units put a block's predecessor in an
+      // earlier wave of the grid, so the ordered additions rarely wait.
+      bh = u % (p.B * p.Hkv);
+      w.n = u / (p.B * p.Hkv);
+    } else {
+      bh = u / nkv;
+      w.n = u % nkv;
+    }
+    w.b = bh / p.Hkv;
+    w.hk = bh % p.Hkv;
   }
-  w.b = bh / p.Hkv;
-  w.hk = bh % p.Hkv;
-  const int nqb = (p.Sq + kBM - 1) / kBM;
+  const int lq = u_lq<PACKED>(w, p), lk = u_lk<PACKED>(w, p);
+  const int nqb = (lq + kBM - 1) / kBM;
   int i0 = 0;
   if (p.causal) {
-    // query row q sees key j iff j <= q + (Sk - Sq); block i reaches key 128 n
-    // iff 64 i + 63 + (Sk - Sq) >= 128 n
-    const int x = kBN * w.n - (p.Sk - p.Sq) - (kBM - 1);
+    // query row q sees key j iff j <= q + (lk - lq); block i reaches key
+    // 128 n iff 64 i + 63 + (lk - lq) >= 128 n
+    const int x = kBN * w.n - (lk - lq) - (kBM - 1);
     i0 = x <= 0 ? 0 : (x + kBM - 1) / kBM;
   }
   w.i0 = i0;
@@ -245,16 +406,17 @@ struct Shared {
 // its dQ^T product is written over the S^T columns of the same buffer.
 constexpr uint32_t kColBuf = 128, kColDPoff = 64, kColDV = 256, kColDK = 384;
 
+template <bool PACKED>
 __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv, const CUtensorMap* tdo, const BwdParams& p,
                               const int total_units) {
   uint32_t sit = 0, ukv = 0;
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<PACKED>(u, p);
     if (w.steps == 0) continue;
     if (!mbar_wait_bounded(sh.kv_empty(), (ukv & 1) ^ 1, sh.abort(), &g_err, kSiteProdKV, p.wait_limit_ns)) return;
     mbar_arrive_expect_tx(sh.kv_full(), 2 * Layout::kKTile);
-    const int krow = w.b * p.Sk + kBN * w.n;
+    const int krow = u_kbase<PACKED>(w, p) + kBN * w.n;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       tma_load_3d(sh.sbase + Layout::kK + c * Layout::kKChunk, tk, sh.kv_full(), c * 64, w.hk, krow);
@@ -268,14 +430,14 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
                              p.wait_limit_ns))
         return;
       mbar_arrive_expect_tx(sh.qd_full(st), 2 * Layout::kQTile + 2 * kBM * 4);
-      const int qrow = w.b * p.Sq + kBM * i;
+      const int qrow = u_qbase<PACKED>(w, p) + kBM * i;
       const uint32_t sb = sh.stage(st);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         tma_load_3d(sb + c * Layout::kQChunk, tq, sh.qd_full(st), c * 64, h, qrow);
         tma_load_3d(sb + Layout::kQTile + c * Layout::kQChunk, tdo, sh.qd_full(st), c * 64, h, qrow);
       }
-      const size_t roff = (size_t(w.b) * p.Hq + h) * p.sq_pad + size_t(kBM) * i;
+      const size_t roff = u_rt<PACKED>(w, p) + size_t(h) * p.sq_pad + size_t(kBM) * i;
       bulk_load(sh.row_terms(st), p.nlse2 + roff, kBM * 4, sh.qd_full(st));
       bulk_load(sh.row_terms(st) + kBM * 4, p.ndelta + roff, kBM * 4, sh.qd_full(st));
     }
@@ -318,6 +480,7 @@ FA_DEV void dq_steps(uint32_t d_dq, uint32_t klo, uint32_t khi, uint32_t slo, ui
 }
 
 // MMA issuer: the whole warp runs this, converged; an elected lane issues.
+template <bool PACKED>
 __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   constexpr uint32_t kIdS = idesc_bf16_f32(kBN, kBM, false, false);   // S^T, dP^T: 128 keys x 64 queries
   constexpr uint32_t kIdG = idesc_bf16_f32(kBN, kD, false, true);     // dV, dK: A in TMEM, B MN-major
@@ -350,7 +513,7 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
   };
 
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<PACKED>(u, p);
     if (w.steps == 0) continue;
     if (!wait(sh.kv_full(), ukv & 1, kSiteMmaKV)) return;
     if (!scores(sit)) return;
@@ -384,6 +547,7 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
 
 // P / dS warpgroup: thread = key row kr of the unit's key block, 64 query
 // columns per step.
+template <bool PACKED>
 __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const BwdParams& p,
                                  const int total_units) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -391,10 +555,9 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
   const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = pk2(sl2, sl2);
-  const int diag = p.Sk - p.Sq;
   uint32_t sit = 0;
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<PACKED>(u, p);
     const int key = kBN * w.n + kr;
     for (int s = 0; s < w.steps; ++s, ++sit) {
       const int i = w.i0 + s % w.nq;
@@ -418,8 +581,8 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
       // columns c < cmin are masked: keys past Sk, or (causal) queries that
       // come before this key
       int cmin = 0;
-      if (key >= p.Sk) cmin = kBM;
-      else if (p.causal) cmin = min(kBM, max(0, key - diag - kBM * i));
+      if (key >= u_lk<PACKED>(w, p)) cmin = kBM;
+      else if (p.causal) cmin = min(kBM, max(0, key - (u_lk<PACKED>(w, p) - u_lq<PACKED>(w, p)) - kBM * i));
       const float2* nl = reinterpret_cast<const float2*>(sh.stage_nlse2(st));
       const float2* nd = reinterpret_cast<const float2*>(sh.stage_ndelta(st));
       uint32_t pp[32], dd[32];
@@ -465,6 +628,7 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
 // two row-major FP32 staging tiles in shared memory (queries 0-31 and 32-63
 // of the block, 32 x 128 each); the reduce issuer adds each into the FP32
 // accumulator.  At the end of a unit it writes dK (scaled) and dV.
+template <bool PACKED>
 __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
@@ -474,7 +638,7 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
   __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk);
   __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<PACKED>(u, p);
     bool stop = false;
     for (int s = 0; s < w.steps; ++s, ++sit) {
       const int buf = sit & 1;
@@ -510,8 +674,8 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
     if (stop || ld_shared_volatile(sh.abort())) break;
     // epilogue of the unit: dV and scale * dK rows in BF16
     const int key = kBN * w.n + d;
-    const bool valid = key < p.Sk;
-    const size_t roff = ((size_t(w.b) * p.Sk + key) * p.Hkv + w.hk) * kD;
+    const bool valid = key < u_lk<PACKED>(w, p);
+    const size_t roff = ((size_t(u_kbase<PACKED>(w, p)) + key) * p.Hkv + w.hk) * kD;
     if (w.steps > 0) {
       if (!mbar_wait_bounded(sh.acc_full(), ukv & 1, sh.abort(), &g_err, kSiteAcc, p.wait_limit_ns)) break;
       tc_fence_after();
@@ -567,6 +731,7 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
 // completion latency of the additions is not paid per step.  Waits point
 // only from key block n to block n - 1 of the same head, and no ticket is
 // held across units (heads), so the waits cannot form a cycle.
+template <bool PACKED>
 __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
   uint32_t sit = 0;
   bool pending1 = false;   // tile 1 of the previous step is still being read
@@ -578,7 +743,7 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
     held = nullptr;
   };
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-    const Unit w = decode_unit(u, p);
+    const Unit w = decode_unit<PACKED>(u, p);
     for (int s = 0; s < w.steps; ++s, ++sit) {
       const int h = w.hk * p.group + s / w.nq;
       const int i = w.i0 + s % w.nq;
@@ -588,7 +753,7 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
         if (!mbar_wait_bounded(sh.dqs_full(half), sit & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns))
           goto done;
         if (p.deterministic && half == 0) {
-          ticket = p.tickets + (size_t(w.b) * p.Hq + h) * p.nqb + i;
+          ticket = p.tickets + u_tk<PACKED>(w, p) + size_t(h) * p.nqb + i;
           const uint64_t t0 = globaltimer_ns();
           while (ld_acquire_gpu(ticket) != w.n) {
             if (ld_shared_volatile(sh.abort()) || globaltimer_ns() - t0 > p.wait_limit_ns) {
@@ -599,7 +764,7 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
             __nanosleep(64);
           }
         }
-        tma_reduce_add_3d(tdq, sh.dq_stage_addr(half), 0, h, w.b * p.Sq + kBM * i + kDqRows * half);
+        tma_reduce_add_3d(tdq, sh.dq_stage_addr(half), 0, h, u_qbase<PACKED>(w, p) + kBM * i + kDqRows * half);
         bulk_commit_group();
         bulk_wait_group_read1();   // every group but this one has been read
         if (half == 0) {
@@ -630,6 +795,7 @@ done:
   if (held) release_held();
 }
 
+template <bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -674,21 +840,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sh.tmem_slot(), 512);
     tmem_relinquish();
   }
-  const int total_units = ((p.Sk + kBN - 1) / kBN) * p.B * p.Hkv;
+  const int total_units = total_units_of<PACKED>(p);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sh.tmem_slot();
   if (warp < 4) {
-    elementwise_role(sh, tmem, p, total_units);
+    elementwise_role<PACKED>(sh, tmem, p, total_units);
   } else if (warp < 8) {
-    dq_role(sh, tmem, p, total_units);
+    dq_role<PACKED>(sh, tmem, p, total_units);
   } else if (warp == 8) {
-    if ((threadIdx.x % 32) == 0) producer_role(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
+    if ((threadIdx.x % 32) == 0) producer_role<PACKED>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
   } else if (warp == 9) {
-    mma_role(sh, tmem, p, total_units);   // converged warp; one elected lane issues
+    mma_role<PACKED>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
   } else if (warp == 10) {
-    if ((threadIdx.x % 32) == 0) reduce_role(sh, &tm_dqacc, p, total_units);
+    if ((threadIdx.x % 32) == 0) reduce_role<PACKED>(sh, &tm_dqacc, p, total_units);
   }
   if (ld_shared_volatile(sh.abort())) {
     const uint64_t t0 = globaltimer_ns();
@@ -707,48 +873,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   const BwdParams& p = L.p;
   if (p.D != bwd::kD) return FA_ERR_UNSUPPORTED;
+  const bool packed = p.cu_seqlens != nullptr;
+  // rows of the [rows, H, D] arrays
+  const int rows_q = packed ? p.Sq : p.B * p.Sq;
+  const int rows_k = packed ? p.Sk : p.B * p.Sk;
   fa_status st;
 
-  // pre: Delta, LSE2, zero accumulator and tickets
-  const long long rows = (long long)p.B * p.Hq * p.sq_pad;
-  const long long n_tickets = p.deterministic ? (long long)p.B * p.Hq * p.nqb * 2 : 0;
+  // pre: (packed: offsets and per-sequence tables,) Delta, LSE2, zero
+  // accumulator and tickets
+  const long long heads_rt = packed ? (long long)p.Hq : (long long)p.B * p.Hq;
+  const long long rows = heads_rt * p.sq_pad;
+  const long long n_tickets = p.deterministic ? heads_rt * p.nqb * 2 : 0;
   long long pre_blocks = (rows * 32 + 255) / 256;
   if (pre_blocks > 16 * L.num_sms) pre_blocks = 16 * L.num_sms;
   if (pre_blocks < 1) pre_blocks = 1;
-  bwd::pre_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
-      p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.B, p.Hq, p.Sq, p.sq_pad);
+  if (packed) {
+    bwd::plan_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.Sq, p.plan);
+    bwd::pre_packed_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
+        p.cu_seqlens, p.plan, p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.B, p.Hq, p.Sq, p.sq_pad);
+  } else {
+    bwd::pre_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
+        p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.B, p.Hq, p.Sq, p.sq_pad);
+  }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
-  if (L.pair) {
+  if (L.pair && !packed) {
     if ((st = launch_bwd_pair_main(L, stream)) != FA_OK) return st;
   } else {
     CUtensorMap tq, tk, tv, tdo, tdq;
-    if ((st = make_tmap_f32_rows_heads_d(&tdq, p.dq_acc, p.B * p.Sq, p.Hq, p.D, p.D, bwd::kDqRows)) != FA_OK)
+    if ((st = make_tmap_f32_rows_heads_d(&tdq, p.dq_acc, rows_q, p.Hq, p.D, p.D, bwd::kDqRows)) != FA_OK)
       return st;
-    if ((st = make_tmap_rows_heads_d(&tq, L.q, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
-    if ((st = make_tmap_rows_heads_d(&tdo, p.dout, p.B * p.Sq, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
-    if ((st = make_tmap_rows_heads_d(&tk, L.k, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
-    if ((st = make_tmap_rows_heads_d(&tv, L.v, p.B * p.Sk, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
+    if ((st = make_tmap_rows_heads_d(&tq, L.q, rows_q, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
+    if ((st = make_tmap_rows_heads_d(&tdo, p.dout, rows_q, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
+    if ((st = make_tmap_rows_heads_d(&tk, L.k, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
+    if ((st = make_tmap_rows_heads_d(&tv, L.v, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
     static bool attr_done = false;
     if (!attr_done) {
-      if (cudaFuncSetAttribute(bwd::bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(bwd::bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bwd::Layout::kDynamic) != cudaSuccess ||
+          cudaFuncSetAttribute(bwd::bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                bwd::Layout::kDynamic) != cudaSuccess)
         return FA_ERR_CUDA;
       attr_done = true;
     }
-    const long long units = (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
+    // packed: the number of key blocks is only known on the device; this
+    // bound (every sequence adds at most one partial block) sizes the grid
+    const long long units = packed ? ((long long)p.Sk / bwd::kBN + p.B) * p.Hkv
+                                   : (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
     const int grid = (int)(units < L.num_sms ? units : L.num_sms);
-    bwd::bwd_kernel<<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+    if (packed)
+      bwd::bwd_kernel<true><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+    else
+      bwd::bwd_kernel<false><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
 
   // post: dQ = BF16(scale * accumulator)
-  const long long n8 = (long long)p.B * p.Sq * p.Hq * p.D / 8;
+  const long long n8 = (long long)rows_q * p.Hq * p.D / 8;
   long long post_blocks = (n8 + 255) / 256;
   if (post_blocks > 16 * L.num_sms) post_blocks = 16 * L.num_sms;
   bwd::post_kernel<<<(unsigned)post_blocks, 256, 0, stream>>>(p.dq_acc, reinterpret_cast<__nv_bfloat16*>(p.dq),
-                                                              n8, p.scale);
+                                                              n8, p.scale, packed ? p.plan + 2 * p.B + 3 : nullptr);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -795,7 +982,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     int Sq, int Sk, int D, int causal, float scale, const int* cu_seqlens,
                                     int deterministic, fa_stream_t stream) {
   try {
-    const size_t need = fa_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic);
+    const size_t need = fa_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, nullptr, cu_seqlens ? Sq : 0, deterministic);
     if (need > FA_BWD_STATIC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0) {  // need == 0: fa_bwd rejects the arguments below, before any launch

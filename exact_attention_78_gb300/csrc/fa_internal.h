@@ -48,10 +48,12 @@ struct BwdParams {
   float* dq_acc;     // [B, Sq, Hq, D] fp32
   float* ndelta;     // [B, Hq, sq_pad]  -sum_d dO * O
   float* nlse2;      // [B, Hq, sq_pad]  -lse * log2(e)
-  int* tickets;      // [B, Hq, nqb, 2] or nullptr
-  int B, Hq, Hkv, Sq, Sk, D;
-  int sq_pad;        // Sq rounded up to a multiple of 64
-  int nqb;           // 64-row query blocks: sq_pad / 64
+  int* tickets;      // [B, Hq, nqb, 2] (packed: [Hq, nqb, 2]) or nullptr
+  const int* cu_seqlens;   // packed layout: device [B + 1]; nullptr for dense
+  int* plan;         // packed: key-block prefix [B + 1], padded-row prefix [B + 1], total key blocks, status
+  int B, Hq, Hkv, Sq, Sk, D;   // packed: Sq = Sk = total rows
+  int sq_pad;        // row-term floats per head: dense Sq rounded up to 64, packed Sq rounded up + 64 B
+  int nqb;           // tickets per head: sq_pad / 64
   int group;
   int causal;
   int deterministic;
@@ -71,9 +73,11 @@ struct BwdLaunch {
 
 // Workspace carve-up of the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {
-  size_t dq_acc, ndelta, nlse2, tickets, total;
+  size_t dq_acc, ndelta, nlse2, plan, tickets, total;
+  int sq_pad;
 };
-BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic);
+// Dense: rows = Sq per batch entry; packed: Sq = total rows of B sequences.
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic, bool packed);
 
 // 3-D tiled tensor map over a [rows, heads, D] BF16 array (D contiguous) with
 // a box of 64 x 1 x box_rows and 128-byte swizzle.

@@ -90,28 +90,38 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
                         int Sq, int Sk, int D, int causal, float scale, const int* cu_seqlens, fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd() needs for this problem (dense layout).
- * The workspace holds the FP32 dQ accumulator [B, Sq, Hq, D], the per-row
- * terms -Delta_i = -sum_d dO_id * O_id and -LSE * log2(e) (FP32
- * [B, Hq, Sq rounded up to a multiple of 64] each) and, when `deterministic`
- * is set, two int32 tickets per (b, h, 64-row query block).  Returns 0 for
- * arguments fa_bwd() would reject (including D != 128).
+ * Bytes of device workspace fa_bwd() needs for this problem.
+ *   Dense layout: cu_seqlens_host = NULL and total_q = 0.  The workspace holds
+ *   the FP32 dQ accumulator [B, Sq, Hq, D], the per-row terms
+ *   -Delta_i = -sum_d dO_id * O_id and -LSE * log2(e) (FP32 [B, Hq, Sq rounded
+ *   up to a multiple of 64] each) and, when `deterministic` is set, two int32
+ *   tickets per (b, h, 64-row query block).
+ *   Packed layout: total_q = the packed row count (the Sq = Sk of the fa_bwd
+ *   call); cu_seqlens_host is an optional HOST copy of the B + 1 offsets,
+ *   checked against the layout rules when given.  The size is a bound that
+ *   does not depend on the individual lengths: FP32 accumulator [total, Hq, D],
+ *   row terms over each sequence's rows rounded up to 64 (Hq x (total rounded
+ *   up to 64 + 64 B) each), the per-sequence offset tables and the tickets.
+ * Returns 0 for arguments fa_bwd() would reject (including D != 128).
  */
-FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int deterministic);
+FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, const int* cu_seqlens_host,
+                                    int total_q, int deterministic);
 
 /*
- * Backward pass of fa_fwd() for the dense layout.  Given the forward inputs,
- * its outputs O and LSE, and the upstream gradient dO, writes dQ, dK, dV
- * (BF16; dK/dV of a key/value head sum over its query-head group).
+ * Backward pass of fa_fwd(), dense or packed layout.  Given the forward
+ * inputs, its outputs O and LSE, and the upstream gradient dO, writes dQ, dK,
+ * dV (BF16; dK/dV of a key/value head sum over its query-head group).
  *   deterministic  0: dQ partial sums are added with FP32 atomics (order may
  *                  vary run to run); 1: they are added in a fixed order so
  *                  repeated calls give bitwise-identical dQ.
  *   workspace      device, 256-byte aligned, at least
- *                  fa_bwd_workspace_size(...) bytes; contents on entry are
- *                  ignored and clobbered.
- * Not built yet, and rejected with FA_ERR_UNSUPPORTED: the packed-length
- * layout (cu_seqlens != NULL) and head dimensions other than 128.
- * Launches three kernels on `stream` (row terms, main pass, dQ conversion).
+ *                  fa_bwd_workspace_size(...) bytes (for the packed layout
+ *                  sized with total_q = Sq); contents on entry are ignored
+ *                  and clobbered.
+ * Head dimensions other than 128 are rejected with FA_ERR_UNSUPPORTED.
+ * Launches three kernels on `stream` (row terms, main pass, dQ conversion),
+ * four for the packed layout (a first one checks the offsets and builds the
+ * per-sequence tables).
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                         const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk,

@@ -76,20 +76,39 @@ def test_forward_tuning_validation(lib):
         assert lib.fa_fwd_ex(A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, 0.125, None, ctypes.byref(bad), None) == 1
 
 
+def _ws(lib, B, Hq, Hkv, Sq, Sk, D, det, total_q=0, offs=None):
+    arr = None if offs is None else (ctypes.c_int * len(offs))(*offs)
+    return lib.fa_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, arr, total_q, det)
+
+
 def test_workspace_size(lib):
-    n = lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 0)
+    n = _ws(lib, 2, 16, 16, 8192, 8192, 128, 0)
     acc = 2 * 8192 * 16 * 128 * 4
     rows = 2 * 16 * 8192 * 4
     assert n == acc + 2 * rows
-    det = lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 1)
+    det = _ws(lib, 2, 16, 16, 8192, 8192, 128, 1)
     assert det == n + 2 * 16 * 128 * 2 * 4      # two tickets (feature halves) per 64-row query block
     # ragged rows: the per-row terms are padded to a multiple of 64 rows
-    r = lib.fa_bwd_workspace_size(1, 2, 2, 100, 100, 128, 0)
+    r = _ws(lib, 1, 2, 2, 100, 100, 128, 0)
     assert r == (1 * 100 * 2 * 128 * 4 + 255) // 256 * 256 + 2 * (1 * 2 * 128 * 4)
-    assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 96, 0) == 0
-    assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 64, 0) == 0
-    assert lib.fa_bwd_workspace_size(2, 15, 4, 8192, 8192, 128, 0) == 0
-    assert lib.fa_bwd_workspace_size(2, 16, 16, 8192, 8192, 128, 3) == 0
+    assert _ws(lib, 2, 16, 16, 8192, 8192, 96, 0) == 0
+    assert _ws(lib, 2, 16, 16, 8192, 8192, 64, 0) == 0
+    assert _ws(lib, 2, 15, 4, 8192, 8192, 128, 0) == 0
+    assert _ws(lib, 2, 16, 16, 8192, 8192, 128, 3) == 0
+
+
+def test_packed_workspace_size(lib):
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    B, H, total = 3, 4, 1000
+    pad = (total + 63) // 64 * 64 + 64 * B          # row terms per head: every sequence rounded up to 64
+    want = al(total * H * 128 * 4) + 2 * al(H * pad * 4) + al((2 * B + 4) * 4)
+    assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total) == want
+    assert _ws(lib, B, H, 2, total, total, 128, 1, total_q=total) == want + al(H * (pad // 64) * 2 * 4)
+    assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total, offs=[0, 10, 700, 1000]) == want
+    assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total, offs=[0, 10, 5, 1000]) == 0     # decreasing
+    assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total, offs=[0, 10, 700, 999]) == 0    # last != total
+    assert _ws(lib, B, H, 2, total, 999, 128, 0, total_q=total) == 0                              # Sk != total
+    assert _ws(lib, 1025, H, 2, total, total, 128, 0, total_q=total) == 0                         # too many sequences
 
 
 def test_backward_rejects_bad_arguments(lib):
@@ -100,7 +119,7 @@ def test_backward_rejects_bad_arguments(lib):
     assert call(det=2) == 1
     assert call(D=80) == 2
     assert call(D=64) == 2
-    assert call(cu=A) == 2
+    assert call(cu=ctypes.c_void_p(A.value + 2)) == 1      # offsets must be 4-byte aligned
     assert call(ws=None) == 5
     assert call(ws=ctypes.c_void_p(A.value + 16)) == 5
     assert call(ws_bytes=100) == 5
