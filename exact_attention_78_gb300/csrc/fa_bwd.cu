@@ -30,8 +30,11 @@
 // longest-first ordering.  The paired-CTA (2-SM) MMA of that bullet is not
 // used here yet: every product runs on one SM's tensor core.
 //
-// Thread layout (384 threads, 12 warps, one CTA per SM):
-//   warps 0-3   P / dS elementwise warpgroup (one thread per key row)
+// Thread layout (512 threads, 16 warps, one CTA per SM; registers per thread
+// after setmaxnreg: elementwise 160, dQ 128, warps 8-11 64):
+//   warps 0-3   P / dS elementwise warpgroup for query columns 0-31 (one
+//               thread per key row)
+//   warps 12-15 the same for query columns 32-63
 //   warps 4-7   dQ warpgroup (dQ^T from TMEM to the staging tiles) and the
 //               dK/dV epilogue
 //   warp  8     TMA producer (one lane)
@@ -39,9 +42,11 @@
 //   warp  10    dQ reduce issuer (one lane; deterministic-mode tickets)
 //   warp  11    idle
 //
-// Tensor memory (512 columns): S^T [0,64) (P^T as BF16 in [0,32)),
-// dP^T [64,128) (dS^T as BF16 in [64,96)), dV [128,256), dK [256,384),
-// dQ^T buffers [384,448) and [448,512).
+// Tensor memory (512 columns): two score buffers b = 0, 1 (steps alternate)
+// with S^T at 128 b and dP^T at 128 b + 64 (P^T / dS^T as BF16 over columns
+// 0-15 and 32-47 of each region, one half per elementwise warpgroup; the dQ^T
+// product is written over S^T once the dV product has read P^T), dV [256, 384),
+// dK [384, 512).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -59,7 +64,7 @@ __device__ DeviceError g_err;
 constexpr int kD = 128;        // head dimension of this kernel
 constexpr int kBN = 128;       // keys per work unit
 constexpr int kBM = 64;        // query rows per step
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kStages = 3;     // Q / dO ring depth
 constexpr int kDqRows = 32;    // rows of the FP32 dQ staging tile (half a query block)
 
@@ -459,13 +464,16 @@ FA_DEV void sdp_steps(uint32_t d_s, uint32_t d_dp, uint32_t klo, uint32_t khi, u
   }
 }
 // Unrolled K steps (64 queries in 16-wide steps) of dV += P^T dO and
-// dK += dS^T Q: A in TMEM (8 columns per step), B MN-major (2048 B per step).
+// dK += dS^T Q: A in TMEM (8 columns per step; queries 0-31 in columns
+// 0-15 and queries 32-63 in columns 32-47 of the region, as the two
+// elementwise warpgroups write them), B MN-major (2048 B per step).
 template <int KK>
 FA_DEV void grad_steps(uint32_t d_dv, uint32_t d_dk, uint32_t a_p, uint32_t a_ds, uint32_t golo, uint32_t gohi,
                        uint32_t qlo, uint32_t qhi, uint32_t idesc, uint32_t acc) {
   if constexpr (KK < kBM / 16) {
-    mma_ts_w<KK * 8, KK * 128>(d_dv, a_p, golo, gohi, idesc, KK > 0 ? 1u : acc);
-    mma_ts_w<KK * 8, KK * 128>(d_dk, a_ds, qlo, qhi, idesc, KK > 0 ? 1u : acc);
+    constexpr uint32_t ca = KK * 8 + (KK >= 2 ? 16 : 0);
+    mma_ts_w<ca, KK * 128>(d_dv, a_p, golo, gohi, idesc, KK > 0 ? 1u : acc);
+    mma_ts_w<ca, KK * 128>(d_dk, a_ds, qlo, qhi, idesc, KK > 0 ? 1u : acc);
     grad_steps<KK + 1>(d_dv, d_dk, a_p, a_ds, golo, gohi, qlo, qhi, idesc, acc);
   }
 }
@@ -545,11 +553,13 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
   }
 }
 
-// P / dS warpgroup: thread = key row kr of the unit's key block, 64 query
-// columns per step.
-template <bool PACKED>
+// P / dS warpgroups: thread = key row kr of the unit's key block; warpgroup
+// H handles query columns [32 H, 32 H + 32) of each 64-row step, so two
+// warpgroups (one warp per scheduler each) share the elementwise work.
+template <bool PACKED, int H>
 __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const BwdParams& p,
                                  const int total_units) {
+  constexpr int kC0 = 32 * H;   // first query column of this warpgroup
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int kr = (warp & 3) * 32 + lane;
   const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
@@ -568,53 +578,50 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
         return;
       tc_fence_after();
       const uint32_t tb = tl + kColBuf * buf;
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tb, sr[0]);
-      tmem_ld32(tb + 32, sr[1]);
-      tmem_ld32(tb + kColDPoff, dr[0]);
-      tmem_ld32(tb + kColDPoff + 32, dr[1]);
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tb + kC0, sr);
+      tmem_ld32(tb + kColDPoff + kC0, dr);
       tmem_ld_wait();
-      tmem_ld_fence(sr[0]);
-      tmem_ld_fence(sr[1]);
-      tmem_ld_fence(dr[0]);
-      tmem_ld_fence(dr[1]);
-      // columns c < cmin are masked: keys past Sk, or (causal) queries that
-      // come before this key
+      tmem_ld_fence(sr);
+      tmem_ld_fence(dr);
+      // columns c < cmin are masked: keys past the sequence's keys, or
+      // (causal) queries that come before this key
       int cmin = 0;
       if (key >= u_lk<PACKED>(w, p)) cmin = kBM;
       else if (p.causal) cmin = min(kBM, max(0, key - (u_lk<PACKED>(w, p) - u_lq<PACKED>(w, p)) - kBM * i));
-      const float2* nl = reinterpret_cast<const float2*>(sh.stage_nlse2(st));
-      const float2* nd = reinterpret_cast<const float2*>(sh.stage_ndelta(st));
-      uint32_t pp[32], dd[32];
+      const float2* nl = reinterpret_cast<const float2*>(sh.stage_nlse2(st) + kC0);
+      const float2* nd = reinterpret_cast<const float2*>(sh.stage_ndelta(st) + kC0);
+      uint32_t pp[16], dd[16];
 #pragma unroll
-      for (int c = 0; c < kBM; c += 2) {
+      for (int c = 0; c < 32; c += 2) {
         const float2 l2 = nl[c / 2], d2 = nd[c / 2];
-        const uint64_t x = fma2(pk2(__uint_as_float(sr[c / 32][c % 32]), __uint_as_float(sr[c / 32][c % 32 + 1])),
-                                sl2x2, pk2(l2.x, l2.y));
+        const uint64_t x = fma2(pk2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, pk2(l2.x, l2.y));
         float x0, x1;
         up2(x, x0, x1);
         float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1);
-        if (c < cmin) p0 = 0.0f;
-        if (c + 1 < cmin) p1 = 0.0f;
-        const uint64_t g = add2(pk2(__uint_as_float(dr[c / 32][c % 32]), __uint_as_float(dr[c / 32][c % 32 + 1])),
-                                pk2(d2.x, d2.y));
+        if (kC0 + c < cmin) p0 = 0.0f;
+        if (kC0 + c + 1 < cmin) p1 = 0.0f;
+        const uint64_t g = add2(pk2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), pk2(d2.x, d2.y));
         float s0, s1;
         up2(mul2(pk2(p0, p1), g), s0, s1);
         pp[c / 2] = pack_bf16x2(p0, p1);
         dd[c / 2] = pack_bf16x2(s0, s1);
       }
-      // P^T and dS^T as BF16 into TMEM (A operands of dV and dK)
-      tmem_st32(tb, pp);
-      tmem_st32(tb + kColDPoff, dd);
+      // P^T and dS^T as BF16 into TMEM (A operands of dV and dK): this
+      // warpgroup's query pairs (32 H + 2 q, 32 H + 2 q + 1) in column 32 H + q
+      // of the S^T / dP^T region -- inside the columns this warpgroup has
+      // just read, never in the other warpgroup's
+      tmem_st16(tb + kC0, pp);
+      tmem_st16(tb + kColDPoff + kC0, dd);
       // dS^T into shared memory (B operand of dQ^T): row kr, 128-byte rows,
-      // 16-byte chunk j stored at chunk j ^ (kr mod 8)
+      // 16-byte chunk j (queries 8 j .. 8 j + 7) stored at chunk j ^ (kr mod 8)
       if (!mbar_wait_bounded(sh.ds_free(buf), ((sit >> 1) & 1) ^ 1, sh.abort(), &g_err, kSiteEsDs,
                              p.wait_limit_ns))
         return;
       uint8_t* row = sh.ds_ptr(buf) + kr * 128;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint4*>(row + ((j ^ (kr & 7)) << 4)) =
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(row + (((4 * H + j) ^ (kr & 7)) << 4)) =
             make_uint4(dd[4 * j], dd[4 * j + 1], dd[4 * j + 2], dd[4 * j + 3]);
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -815,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(sh.s_full(b), 1);
-      mbar_init(sh.p_ready(b), 128);
+      mbar_init(sh.p_ready(b), 256);
       mbar_init(sh.dq_full(b), 1);
       mbar_init(sh.dq_empty(b), 128);
       mbar_init(sh.ds_free(b), 1);
@@ -845,16 +852,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sh.tmem_slot();
+  // register split (sums to the 512 x 128 the block was launched with)
   if (warp < 4) {
-    elementwise_role<PACKED>(sh, tmem, p, total_units);
+    reg_alloc<160>();
+    elementwise_role<PACKED, 0>(sh, tmem, p, total_units);
   } else if (warp < 8) {
     dq_role<PACKED>(sh, tmem, p, total_units);
-  } else if (warp == 8) {
-    if ((threadIdx.x % 32) == 0) producer_role<PACKED>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
-  } else if (warp == 9) {
-    mma_role<PACKED>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
-  } else if (warp == 10) {
-    if ((threadIdx.x % 32) == 0) reduce_role<PACKED>(sh, &tm_dqacc, p, total_units);
+  } else if (warp < 12) {
+    reg_dealloc<64>();
+    if (warp == 8) {
+      if ((threadIdx.x % 32) == 0) producer_role<PACKED>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
+    } else if (warp == 9) {
+      mma_role<PACKED>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
+    } else if (warp == 10) {
+      if ((threadIdx.x % 32) == 0) reduce_role<PACKED>(sh, &tm_dqacc, p, total_units);
+    }
+  } else {
+    reg_alloc<160>();
+    elementwise_role<PACKED, 1>(sh, tmem, p, total_units);
   }
   if (ld_shared_volatile(sh.abort())) {
     const uint64_t t0 = globaltimer_ns();
