@@ -45,8 +45,8 @@
 // Tensor memory (512 columns): two score buffers b = 0, 1 (steps alternate)
 // with S^T at 128 b and dP^T at 128 b + 64 (P^T / dS^T as BF16 over columns
 // 0-15 and 32-47 of each region, one half per elementwise warpgroup; the dQ^T
-// product is written over S^T once the dV product has read P^T), dV [256, 384),
-// dK [384, 512).
+// product is written over dP^T once the dK product has read dS^T), dV
+// [256, 384), dK [384, 512).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -407,8 +407,9 @@ struct Shared {
 };
 
 // TMEM columns.  Two score buffers b = 0, 1 (steps alternate): S^T at
-// 128 b, dP^T at 128 b + 64.  After a step's P^T / dS^T have been consumed,
-// its dQ^T product is written over the S^T columns of the same buffer.
+// 128 b, dP^T at 128 b + 64.  After a step's dS^T has been consumed by the dK
+// product, its dQ^T product is written over the dP^T columns of the same
+// buffer, so the next S^T into the buffer need not wait for its read-out.
 constexpr uint32_t kColBuf = 128, kColDPoff = 64, kColDV = 256, kColDK = 384;
 
 template <bool PACKED>
@@ -450,17 +451,15 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
   }
 }
 
-// Unrolled K steps (K = D in 16-wide steps) of S^T = K Q^T and dP^T = V dO^T;
-// all operands K-major: step kk reads 64-wide chunk kk/4 at byte 32*(kk%4).
+// Unrolled K steps (K = D in 16-wide steps) of S^T = K Q^T or dP^T = V dO^T;
+// both operands K-major: step kk reads 64-wide chunk kk/4 at byte 32*(kk%4).
 template <int KK>
-FA_DEV void sdp_steps(uint32_t d_s, uint32_t d_dp, uint32_t klo, uint32_t khi, uint32_t vlo, uint32_t vhi,
-                      uint32_t qlo, uint32_t qhi, uint32_t glo, uint32_t ghi, uint32_t idesc) {
+FA_DEV void score_steps(uint32_t d, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi, uint32_t idesc) {
   if constexpr (KK < kD / 16) {
     constexpr uint32_t oa = ((KK >> 2) * Layout::kKChunk + (KK & 3) * 32) >> 4;
     constexpr uint32_t ob = ((KK >> 2) * Layout::kQChunk + (KK & 3) * 32) >> 4;
-    mma_ss_w<oa, ob>(d_s, klo, khi, qlo, qhi, idesc, KK > 0 ? 1u : 0u);
-    mma_ss_w<oa, ob>(d_dp, vlo, vhi, glo, ghi, idesc, KK > 0 ? 1u : 0u);
-    sdp_steps<KK + 1>(d_s, d_dp, klo, khi, vlo, vhi, qlo, qhi, glo, ghi, idesc);
+    mma_ss_w<oa, ob>(d, alo, ahi, blo, bhi, idesc, KK > 0 ? 1u : 0u);
+    score_steps<KK + 1>(d, alo, ahi, blo, bhi, idesc);
   }
 }
 // Unrolled K steps (64 queries in 16-wide steps) of dV += P^T dO and
@@ -503,19 +502,21 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
     tc_fence_after();
     return true;
   };
-  auto issue_sdp = [&](int st, int buf) {
-    const uint64_t dq = sdesc_sw128(sh.stage(st), 16, 1024);
-    const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout::kQTile, 16, 1024);
-    sdp_steps<0>(tmem + kColBuf * buf, tmem + kColBuf * buf + kColDPoff, desc_lo(dk_kmaj), desc_hi(dk_kmaj),
-                 desc_lo(dv_kmaj), desc_hi(dv_kmaj), desc_lo(dq), desc_hi(dq), desc_lo(dg), desc_hi(dg), kIdS);
-  };
-  // Scores of global step t into buffer t & 1, once the dQ^T written there
-  // by step t - 2 has been read out.
+  // Scores of global step t into buffer t & 1: S^T at once, dP^T once the
+  // dQ^T written over the dP^T columns by step t - 2 has been read out (so
+  // the S^T product covers that read-out).  Deterministic mode waits for the
+  // read-out first: its dQ warpgroup is paced by the ordered additions, and
+  // queueing S^T ahead of that wait measured slower there.
   auto scores = [&](uint32_t t) -> bool {
-    const int buf = t & 1;
-    if (!wait(sh.qd_full(t % kStages), (t / kStages) & 1, kSiteMmaQ)) return false;
-    if (!wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
-    issue_sdp(t % kStages, buf);
+    const int buf = t & 1, st = t % kStages;
+    if (!wait(sh.qd_full(st), (t / kStages) & 1, kSiteMmaQ)) return false;
+    if (p.deterministic && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
+    const uint64_t dq = sdesc_sw128(sh.stage(st), 16, 1024);
+    score_steps<0>(tmem + kColBuf * buf, desc_lo(dk_kmaj), desc_hi(dk_kmaj), desc_lo(dq), desc_hi(dq), kIdS);
+    if (!p.deterministic && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
+    const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout::kQTile, 16, 1024);
+    score_steps<0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dv_kmaj), desc_hi(dv_kmaj), desc_lo(dg), desc_hi(dg),
+                   kIdS);
     mma_commit_w(sh.s_full(buf));
     return true;
   };
@@ -539,11 +540,12 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
       grad_steps<0>(tmem + kColDV, tmem + kColDK, tmem + kColBuf * buf, tmem + kColBuf * buf + kColDPoff,
                     desc_lo(dgo), desc_hi(dgo), desc_lo(dqq), desc_hi(dqq), kIdG, s > 0 ? 1u : 0u);
       mma_commit_w(sh.qd_empty(st));
-      // dQ_i^T = K^T dS^T over the S^T columns of this buffer (its P^T has
-      // just been read by the dV product, issued before): M = D (K MN-major,
+      // dQ_i^T = K^T dS^T over the dP^T columns of this buffer (its dS^T has
+      // just been read by the dK product, issued before): M = D (K MN-major,
       // chunks 16 KB apart), N = 64 queries (dS^T MN-major), K = 128 keys
       const uint64_t dsd = sdesc_sw128(sh.ds(buf), Layout::kDsBytes, 1024);
-      dq_steps<0>(tmem + kColBuf * buf, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd), kIdQ);
+      dq_steps<0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd),
+                  kIdQ);
       mma_commit_w(sh.dq_full(buf));
       mma_commit_w(sh.ds_free(buf));
     }
@@ -655,8 +657,8 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
       }
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(tl + kColBuf * buf, v[0]);
-      tmem_ld32(tl + kColBuf * buf + 32, v[1]);
+      tmem_ld32(tl + kColBuf * buf + kColDPoff, v[0]);
+      tmem_ld32(tl + kColBuf * buf + kColDPoff + 32, v[1]);
       tmem_ld_wait();
       tmem_ld_fence(v[0]);
       tmem_ld_fence(v[1]);
