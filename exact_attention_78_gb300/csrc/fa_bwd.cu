@@ -88,8 +88,8 @@ struct Layout {
   static constexpr int kRowTerms = kDqStage + 2 * kDqStageBytes;  // [kStages][2][kBM] floats
   static constexpr int kBars = kRowTerms + kStages * kRowTermBytes;
   // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full[2], p_ready[2],
-  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full[2], dqs_free[2]
-  static constexpr int kNumBars = 2 + 2 * kStages + 10 + 2 + 4;
+  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full[2], dqs_free[2], q_full[S]
+  static constexpr int kNumBars = 2 + 2 * kStages + 10 + 2 + 4 + kStages;
   static constexpr int kMisc = kBars + kNumBars * 8;              // tmem slot, abort, check-in count
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kDynamic = kTotal + kSmemAlignSlack;
@@ -376,7 +376,8 @@ struct Shared {
   FA_DEV uint32_t bar(int i) const { return sbase + L::kBars + 8 * i; }
   FA_DEV uint32_t kv_full() const { return bar(0); }
   FA_DEV uint32_t kv_empty() const { return bar(1); }
-  FA_DEV uint32_t qd_full(int s) const { return bar(2 + s); }
+  FA_DEV uint32_t qd_full(int s) const { return bar(2 + s); }   // dO and the row terms landed
+  FA_DEV uint32_t q_full(int s) const { return bar(18 + 2 * kStages + s); }   // Q landed
   FA_DEV uint32_t qd_empty(int s) const { return bar(2 + kStages + s); }
   // per TMEM score buffer b (steps alternate buffers)
   FA_DEV uint32_t s_full(int b) const { return bar(2 + 2 * kStages + b); }
@@ -435,14 +436,17 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
       if (!mbar_wait_bounded(sh.qd_empty(st), ((sit / kStages) & 1) ^ 1, sh.abort(), &g_err, kSiteProdQ,
                              p.wait_limit_ns))
         return;
-      mbar_arrive_expect_tx(sh.qd_full(st), 2 * Layout::kQTile + 2 * kBM * 4);
+      // Q on its own barrier (the S^T product needs nothing else), then dO
+      // and the row terms
+      mbar_arrive_expect_tx(sh.q_full(st), Layout::kQTile);
+      mbar_arrive_expect_tx(sh.qd_full(st), Layout::kQTile + 2 * kBM * 4);
       const int qrow = u_qbase<PACKED>(w, p) + kBM * i;
       const uint32_t sb = sh.stage(st);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tma_load_3d(sb + c * Layout::kQChunk, tq, sh.qd_full(st), c * 64, h, qrow);
+      for (int c = 0; c < 2; ++c) tma_load_3d(sb + c * Layout::kQChunk, tq, sh.q_full(st), c * 64, h, qrow);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
         tma_load_3d(sb + Layout::kQTile + c * Layout::kQChunk, tdo, sh.qd_full(st), c * 64, h, qrow);
-      }
       const size_t roff = u_rt<PACKED>(w, p) + size_t(h) * p.sq_pad + size_t(kBM) * i;
       bulk_load(sh.row_terms(st), p.nlse2 + roff, kBM * 4, sh.qd_full(st));
       bulk_load(sh.row_terms(st) + kBM * 4, p.ndelta + roff, kBM * 4, sh.qd_full(st));
@@ -509,11 +513,13 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
   // queueing S^T ahead of that wait measured slower there.
   auto scores = [&](uint32_t t) -> bool {
     const int buf = t & 1, st = t % kStages;
-    if (!wait(sh.qd_full(st), (t / kStages) & 1, kSiteMmaQ)) return false;
+    const uint32_t ph = (t / kStages) & 1;
+    if (!wait(sh.q_full(st), ph, kSiteMmaQ)) return false;
     if (p.deterministic && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
     const uint64_t dq = sdesc_sw128(sh.stage(st), 16, 1024);
     score_steps<0>(tmem + kColBuf * buf, desc_lo(dk_kmaj), desc_hi(dk_kmaj), desc_lo(dq), desc_hi(dq), kIdS);
     if (!p.deterministic && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
+    if (!wait(sh.qd_full(st), ph, kSiteMmaQ)) return false;
     const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout::kQTile, 16, 1024);
     score_steps<0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dv_kmaj), desc_hi(dv_kmaj), desc_lo(dg), desc_hi(dg),
                    kIdS);
@@ -820,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sh.kv_empty(), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(sh.qd_full(s), 1);
+      mbar_init(sh.q_full(s), 1);
       mbar_init(sh.qd_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
