@@ -114,6 +114,8 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministi
   off = align256(off + heads_rt * sq_pad * sizeof(float));
   w.plan = off;
   if (packed) off = align256(off + (2 * size_t(B) + 4) * sizeof(int));
+  w.sched = off;
+  off = align256(off + sizeof(int));
   w.tickets = off;
   if (deterministic) off = align256(off + heads_rt * (sq_pad / 64) * 2 * sizeof(int));
   w.total = off;
@@ -261,6 +263,30 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.tickets = deterministic ? reinterpret_cast<int*>(wb + ws.tickets) : nullptr;
     L.p.cu_seqlens = cu_seqlens;
     L.p.plan = packed ? reinterpret_cast<int*>(wb + ws.plan) : nullptr;
+    L.p.sched = reinterpret_cast<int*>(wb + ws.sched);
+    // Work schedule of the main kernel (see its decode_unit and
+    // producer_role).  Units are claimed dynamically where their lengths
+    // differ enough for a static round-robin to leave SMs idle at the end
+    // (packed sequences, causal masks over short sequences) and in the
+    // deterministic mode; otherwise CTA c takes units c, c + grid, ... in
+    // head-major order, which measured faster for uniform units (it keeps a
+    // head's key blocks on neighbouring CTAs).  Dense order: head-major
+    // (g = 1); longest first within groups of heads for dynamic causal runs,
+    // the group sized so that the groups in flight keep their Q, dO, K, V and
+    // dQ-accumulator rows (~1.5 KB per row) in L2; deterministic mode:
+    // key-block-major over all heads.
+    {
+      const long long bh = (long long)B * Hkv;
+      const bool dynamic = packed || deterministic || (causal && Sk <= 2048);
+      long long g = 1;
+      if (deterministic) g = bh;
+      else if (dynamic && causal) g = (64ll << 20) / ((long long)Sk * 1536);
+      if (g < 1) g = 1;
+      if (g > 16 && !deterministic) g = 16;
+      if (g > bh) g = bh;
+      L.p.sched_group = (int)g;
+      L.p.sched_dynamic = dynamic ? 1 : 0;
+    }
     L.p.B = B;
     L.p.Hq = Hq;
     L.p.Hkv = Hkv;

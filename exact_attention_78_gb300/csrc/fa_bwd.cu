@@ -67,6 +67,10 @@ constexpr int kBM = 64;        // query rows per step
 constexpr int kThreads = 512;
 constexpr int kStages = 3;     // Q / dO ring depth
 constexpr int kDqRows = 32;    // rows of the FP32 dQ staging tile (half a query block)
+constexpr int kRing = 4;       // work units announced ahead by the producer
+// consumers of each announced unit: two elementwise warpgroups, the dQ
+// warpgroup, the MMA warp and the reduce issuer
+constexpr int kRingReaders = 128 + 128 + 128 + 32 + 1;
 
 enum Site { kSiteEsS = 1, kSiteEsQ, kSiteEsDs, kSiteDqFull, kSiteDqTicket, kSiteAcc, kSiteMmaKV, kSiteMmaQ,
             kSiteMmaP, kSiteMmaDq, kSiteMmaAcc, kSiteProdKV, kSiteProdQ };
@@ -88,8 +92,9 @@ struct Layout {
   static constexpr int kRowTerms = kDqStage + 2 * kDqStageBytes;  // [kStages][2][kBM] floats
   static constexpr int kBars = kRowTerms + kStages * kRowTermBytes;
   // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full[2], p_ready[2],
-  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full[2], dqs_free[2], q_full[S]
-  static constexpr int kNumBars = 2 + 2 * kStages + 10 + 2 + 4 + kStages;
+  // dq_full[2], dq_empty[2], ds_free[2], acc_full, acc_empty, dqs_full[2], dqs_free[2], q_full[S],
+  // unit ring full[4] / empty[4]
+  static constexpr int kNumBars = 2 + 2 * kStages + 10 + 2 + 4 + kStages + 2 * kRing;
   static constexpr int kMisc = kBars + kNumBars * 8;              // tmem slot, abort, check-in count
   static constexpr int kTotal = kMisc + 64;
   static constexpr int kDynamic = kTotal + kSmemAlignSlack;
@@ -104,8 +109,9 @@ struct Layout {
 // (LSE = -inf) get -inf and 0, so their weights come out as exactly 0.
 __global__ void pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                            const float* __restrict__ lse, float* __restrict__ ndelta, float* __restrict__ nlse2,
-                           float* __restrict__ dq_acc, int* __restrict__ tickets, long long n_tickets, int B,
-                           int Hq, int Sq, int sq_pad) {
+                           float* __restrict__ dq_acc, int* __restrict__ tickets, long long n_tickets,
+                           int* __restrict__ sched, int B, int Hq, int Sq, int sq_pad) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;   // work-unit counter of the main kernel
   const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)B * Hq * sq_pad;
@@ -224,7 +230,9 @@ __global__ void pre_packed_kernel(const __nv_bfloat16* __restrict__ o, const __n
                                   const float* __restrict__ lse, const int* __restrict__ cu,
                                   const int* __restrict__ plan, float* __restrict__ ndelta,
                                   float* __restrict__ nlse2, float* __restrict__ dq_acc, int* __restrict__ tickets,
-                                  long long n_tickets, int B, int Hq, int total, int sq_pad) {
+                                  long long n_tickets, int* __restrict__ sched, int B, int Hq, int total,
+                                  int sq_pad) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;   // work-unit counter of the main kernel
   if (plan[2 * B + 3] != 0) return;   // offsets rejected: nothing is computed
   const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -334,23 +342,21 @@ __device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p) {
     w.rt = p.plan[p.B + 1 + lo];   // padded-row prefix (multiple of 64)
     w.tk = w.rt / kBM;
   } else {
-    // Head-major: the key blocks of one (batch, kv head) are adjacent, so
-    // the CTAs working at the same time share that head's Q / dO reads and
-    // its slice of the dQ accumulator in L2.  Within a head, key blocks
-    // come in ascending order: under a causal mask the early blocks see the
-    // most query rows, so each head's longest units come first.
+    // Units in groups of g = sched_group (batch, kv head) pairs; within a
+    // group key block n ascends, each n over the group's heads.  Under a
+    // causal mask block n sees the most query rows when n is small, so the
+    // order is longest first within each group, and the units being worked
+    // on at one time touch only a few heads' Q / dO rows and dQ-accumulator
+    // slices (L2 reuse).  g = 1 is head-major (no mask: all units equally
+    // long); deterministic mode uses g = all heads (key-block-major), which
+    // puts a block's predecessor in the ordered dQ additions far ahead.
     const int nkv = (p.Sk + kBN - 1) / kBN;
-    int bh;
-    if (p.deterministic) {
-      // Deterministic mode orders each (b, h, query block)'s dQ additions by
-      // key block; key-block-major units put a block's predecessor in an
-      // earlier wave of the grid, so the ordered additions rarely wait.
-      bh = u % (p.B * p.Hkv);
-      w.n = u / (p.B * p.Hkv);
-    } else {
-      bh = u / nkv;
-      w.n = u % nkv;
-    }
+    const int nbh = p.B * p.Hkv;
+    const int g = p.sched_group;
+    const int grp = u / (g * nkv), r = u % (g * nkv);
+    const int gh = min(g, nbh - grp * g);   // heads in this (possibly last, smaller) group
+    const int bh = grp * g + r % gh;
+    w.n = r / gh;
     w.b = bh / p.Hkv;
     w.hk = bh % p.Hkv;
   }
@@ -378,6 +384,9 @@ struct Shared {
   FA_DEV uint32_t kv_empty() const { return bar(1); }
   FA_DEV uint32_t qd_full(int s) const { return bar(2 + s); }   // dO and the row terms landed
   FA_DEV uint32_t q_full(int s) const { return bar(18 + 2 * kStages + s); }   // Q landed
+  FA_DEV uint32_t ring_full(int r) const { return bar(18 + 3 * kStages + r); }
+  FA_DEV uint32_t ring_empty(int r) const { return bar(18 + 3 * kStages + kRing + r); }
+  FA_DEV uint32_t ring(int r) const { return sbase + L::kMisc + 16 + 4 * r; }   // announced unit indices
   FA_DEV uint32_t qd_empty(int s) const { return bar(2 + kStages + s); }
   // per TMEM score buffer b (steps alternate buffers)
   FA_DEV uint32_t s_full(int b) const { return bar(2 + 2 * kStages + b); }
@@ -413,12 +422,44 @@ struct Shared {
 // buffer, so the next S^T into the buffer need not wait for its read-out.
 constexpr uint32_t kColBuf = 128, kColDPoff = 64, kColDV = 256, kColDK = 384;
 
-template <bool PACKED>
+// Work schedule.  Static: CTA c takes units c, c + grid, ...  Dynamic: the
+// producer claims units from a counter in global memory (atomicAdd, so SMs
+// that finish early take more) and announces them, in claim order, through
+// a small ring in shared memory that every other role reads.  -1 ends it.
+template <bool DYN>
+FA_DEV int next_unit(const Shared& sh, int k, const BwdParams& p, int site, int total_units) {
+  if constexpr (!DYN) {
+    const int u = (int)blockIdx.x + k * (int)gridDim.x;
+    return u < total_units ? u : -1;
+  }
+  const int slot = k % kRing;
+  if (!mbar_wait_bounded(sh.ring_full(slot), (k / kRing) & 1, sh.abort(), &g_err, site, p.wait_limit_ns)) return -1;
+  const int u = ld_shared_volatile(sh.ring(slot));
+  mbar_arrive(sh.ring_empty(slot));
+  return u;
+}
+
+template <bool PACKED, bool DYN>
 __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv, const CUtensorMap* tdo, const BwdParams& p,
                               const int total_units) {
   uint32_t sit = 0, ukv = 0;
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int k = 0;; ++k) {
+    int u;
+    if constexpr (DYN) {
+      u = atomicAdd(p.sched, 1);
+      if (u < 0 || u >= total_units) u = -1;
+      const int slot = k % kRing;
+      if (!mbar_wait_bounded(sh.ring_empty(slot), ((k / kRing) & 1) ^ 1, sh.abort(), &g_err, kSiteProdKV,
+                             p.wait_limit_ns))
+        return;
+      st_shared(sh.ring(slot), u);
+      mbar_arrive(sh.ring_full(slot));
+    } else {
+      u = (int)blockIdx.x + k * (int)gridDim.x;
+      if (u >= total_units) u = -1;
+    }
+    if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     if (w.steps == 0) continue;
     if (!mbar_wait_bounded(sh.kv_empty(), (ukv & 1) ^ 1, sh.abort(), &g_err, kSiteProdKV, p.wait_limit_ns)) return;
@@ -491,7 +532,7 @@ FA_DEV void dq_steps(uint32_t d_dq, uint32_t klo, uint32_t khi, uint32_t slo, ui
 }
 
 // MMA issuer: the whole warp runs this, converged; an elected lane issues.
-template <bool PACKED>
+template <bool PACKED, bool DYN>
 __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   constexpr uint32_t kIdS = idesc_bf16_f32(kBN, kBM, false, false);   // S^T, dP^T: 128 keys x 64 queries
   constexpr uint32_t kIdG = idesc_bf16_f32(kBN, kD, false, true);     // dV, dK: A in TMEM, B MN-major
@@ -527,7 +568,9 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
     return true;
   };
 
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int k = 0;; ++k) {
+    const int u = next_unit<DYN>(sh, k, p, kSiteMmaKV, total_units);
+    if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     if (w.steps == 0) continue;
     if (!wait(sh.kv_full(), ukv & 1, kSiteMmaKV)) return;
@@ -564,7 +607,7 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
 // P / dS warpgroups: thread = key row kr of the unit's key block; warpgroup
 // H handles query columns [32 H, 32 H + 32) of each 64-row step, so two
 // warpgroups (one warp per scheduler each) share the elementwise work.
-template <bool PACKED, int H>
+template <bool PACKED, bool DYN, int H>
 __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const BwdParams& p,
                                  const int total_units) {
   constexpr int kC0 = 32 * H;   // first query column of this warpgroup
@@ -574,7 +617,9 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = pk2(sl2, sl2);
   uint32_t sit = 0;
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int k = 0;; ++k) {
+    const int u = next_unit<DYN>(sh, k, p, kSiteEsQ, total_units);
+    if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     const int key = kBN * w.n + kr;
     for (int s = 0; s < w.steps; ++s, ++sit) {
@@ -643,7 +688,7 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
 // two row-major FP32 staging tiles in shared memory (queries 0-31 and 32-63
 // of the block, 32 x 128 each); the reduce issuer adds each into the FP32
 // accumulator.  At the end of a unit it writes dK (scaled) and dV.
-template <bool PACKED>
+template <bool PACKED, bool DYN>
 __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
@@ -652,7 +697,9 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
   uint32_t sit = 0, ukv = 0;
   __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk);
   __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int k = 0;; ++k) {
+    const int u = next_unit<DYN>(sh, k, p, kSiteDqFull, total_units);
+    if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     bool stop = false;
     for (int s = 0; s < w.steps; ++s, ++sit) {
@@ -746,7 +793,7 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
 // completion latency of the additions is not paid per step.  Waits point
 // only from key block n to block n - 1 of the same head, and no ticket is
 // held across units (heads), so the waits cannot form a cycle.
-template <bool PACKED>
+template <bool PACKED, bool DYN>
 __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
   uint32_t sit = 0;
   bool pending1 = false;   // tile 1 of the previous step is still being read
@@ -757,7 +804,9 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
     st_release_gpu(held, held_next);
     held = nullptr;
   };
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int k = 0;; ++k) {
+    const int u = next_unit<DYN>(sh, k, p, kSiteDqFull, total_units);
+    if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     for (int s = 0; s < w.steps; ++s, ++sit) {
       const int h = w.hk * p.group + s / w.nq;
@@ -810,7 +859,7 @@ done:
   if (held) release_held();
 }
 
-template <bool PACKED>
+template <bool PACKED, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -842,6 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sh.dqs_full(b), 128);
       mbar_init(sh.dqs_free(b), 1);
     }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(sh.ring_full(r), 1);
+      mbar_init(sh.ring_empty(r), kRingReaders);
+    }
     st_shared(sh.abort(), 0);
     fence_barrier_init();
   }
@@ -864,21 +917,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // register split (sums to the 512 x 128 the block was launched with)
   if (warp < 4) {
     reg_alloc<160>();
-    elementwise_role<PACKED, 0>(sh, tmem, p, total_units);
+    elementwise_role<PACKED, DYN, 0>(sh, tmem, p, total_units);
   } else if (warp < 8) {
-    dq_role<PACKED>(sh, tmem, p, total_units);
+    dq_role<PACKED, DYN>(sh, tmem, p, total_units);
   } else if (warp < 12) {
     reg_dealloc<64>();
     if (warp == 8) {
-      if ((threadIdx.x % 32) == 0) producer_role<PACKED>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
+      if ((threadIdx.x % 32) == 0) producer_role<PACKED, DYN>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
     } else if (warp == 9) {
-      mma_role<PACKED>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
+      mma_role<PACKED, DYN>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
     } else if (warp == 10) {
-      if ((threadIdx.x % 32) == 0) reduce_role<PACKED>(sh, &tm_dqacc, p, total_units);
+      if ((threadIdx.x % 32) == 0) reduce_role<PACKED, DYN>(sh, &tm_dqacc, p, total_units);
     }
   } else {
     reg_alloc<160>();
-    elementwise_role<PACKED, 1>(sh, tmem, p, total_units);
+    elementwise_role<PACKED, DYN, 1>(sh, tmem, p, total_units);
   }
   if (ld_shared_volatile(sh.abort())) {
     const uint64_t t0 = globaltimer_ns();
@@ -915,11 +968,12 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
     bwd::plan_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.Sq, p.plan);
     bwd::pre_packed_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
-        p.cu_seqlens, p.plan, p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.B, p.Hq, p.Sq, p.sq_pad);
+        p.cu_seqlens, p.plan, p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq,
+        p.sq_pad);
   } else {
     bwd::pre_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
-        p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.B, p.Hq, p.Sq, p.sq_pad);
+        p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq, p.sq_pad);
   }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
@@ -935,9 +989,11 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
     if ((st = make_tmap_rows_heads_d(&tv, L.v, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
     static bool attr_done = false;
     if (!attr_done) {
-      if (cudaFuncSetAttribute(bwd::bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(bwd::bwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                bwd::Layout::kDynamic) != cudaSuccess ||
-          cudaFuncSetAttribute(bwd::bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          cudaFuncSetAttribute(bwd::bwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bwd::Layout::kDynamic) != cudaSuccess ||
+          cudaFuncSetAttribute(bwd::bwd_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                bwd::Layout::kDynamic) != cudaSuccess)
         return FA_ERR_CUDA;
       attr_done = true;
@@ -947,10 +1003,15 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
     const long long units = packed ? ((long long)p.Sk / bwd::kBN + p.B) * p.Hkv
                                    : (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
     const int grid = (int)(units < L.num_sms ? units : L.num_sms);
+    // packed layouts always use the dynamic schedule (their units differ in
+    // length); dense ones as chosen by the caller (sched_dynamic)
     if (packed)
-      bwd::bwd_kernel<true><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+      bwd::bwd_kernel<true, true><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+    else if (p.sched_dynamic)
+      bwd::bwd_kernel<false, true><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
     else
-      bwd::bwd_kernel<false><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+      bwd::bwd_kernel<false, false><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq,
+                                                                                          p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
 

@@ -51,6 +51,9 @@ struct BwdParams {
   int* tickets;      // [B, Hq, nqb, 2] (packed: [Hq, nqb, 2]) or nullptr
   const int* cu_seqlens;   // packed layout: device [B + 1]; nullptr for dense
   int* plan;         // packed: key-block prefix [B + 1], padded-row prefix [B + 1], total key blocks, status
+  int* sched;        // work-unit counter of the dynamic scheduler (zeroed by the pre pass)
+  int sched_group;   // dense: heads per group of the longest-first unit order
+  int sched_dynamic; // 1: units claimed from the counter; 0: CTA c takes units c, c + grid, ...
   int B, Hq, Hkv, Sq, Sk, D;   // packed: Sq = Sk = total rows
   int sq_pad;        // row-term floats per head: dense Sq rounded up to 64, packed Sq rounded up + 64 B
   int nqb;           // tickets per head: sq_pad / 64
@@ -73,7 +76,7 @@ struct BwdLaunch {
 
 // Workspace carve-up of the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {
-  size_t dq_acc, ndelta, nlse2, plan, tickets, total;
+  size_t dq_acc, ndelta, nlse2, plan, sched, tickets, total;
   int sq_pad;
 };
 // Dense: rows = Sq per batch entry; packed: Sq = total rows of B sequences.

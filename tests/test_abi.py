@@ -85,12 +85,12 @@ def test_workspace_size(lib):
     n = _ws(lib, 2, 16, 16, 8192, 8192, 128, 0)
     acc = 2 * 8192 * 16 * 128 * 4
     rows = 2 * 16 * 8192 * 4
-    assert n == acc + 2 * rows
+    assert n == acc + 2 * rows + 256                # + the scheduler's work counter
     det = _ws(lib, 2, 16, 16, 8192, 8192, 128, 1)
     assert det == n + 2 * 16 * 128 * 2 * 4      # two tickets (feature halves) per 64-row query block
     # ragged rows: the per-row terms are padded to a multiple of 64 rows
     r = _ws(lib, 1, 2, 2, 100, 100, 128, 0)
-    assert r == (1 * 100 * 2 * 128 * 4 + 255) // 256 * 256 + 2 * (1 * 2 * 128 * 4)
+    assert r == (1 * 100 * 2 * 128 * 4 + 255) // 256 * 256 + 2 * (1 * 2 * 128 * 4) + 256
     assert _ws(lib, 2, 16, 16, 8192, 8192, 96, 0) == 0
     assert _ws(lib, 2, 16, 16, 8192, 8192, 64, 0) == 0
     assert _ws(lib, 2, 15, 4, 8192, 8192, 128, 0) == 0
@@ -101,7 +101,7 @@ def test_packed_workspace_size(lib):
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     B, H, total = 3, 4, 1000
     pad = (total + 63) // 64 * 64 + 64 * B          # row terms per head: every sequence rounded up to 64
-    want = al(total * H * 128 * 4) + 2 * al(H * pad * 4) + al((2 * B + 4) * 4)
+    want = al(total * H * 128 * 4) + 2 * al(H * pad * 4) + al((2 * B + 4) * 4) + 256
     assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total) == want
     assert _ws(lib, B, H, 2, total, total, 128, 1, total_q=total) == want + al(H * (pad // 64) * 2 * 4)
     assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total, offs=[0, 10, 700, 1000]) == want
