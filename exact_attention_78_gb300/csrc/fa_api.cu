@@ -265,22 +265,23 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.plan = packed ? reinterpret_cast<int*>(wb + ws.plan) : nullptr;
     L.p.sched = reinterpret_cast<int*>(wb + ws.sched);
     // Work schedule of the main kernel (see its decode_unit and
-    // producer_role).  Units are claimed dynamically where their lengths
-    // differ enough for a static round-robin to leave SMs idle at the end
-    // (packed sequences, causal masks over short sequences) and in the
-    // deterministic mode; otherwise CTA c takes units c, c + grid, ... in
-    // head-major order, which measured faster for uniform units (it keeps a
-    // head's key blocks on neighbouring CTAs).  Dense order: head-major
-    // (g = 1); longest first within groups of heads for dynamic causal runs,
-    // the group sized so that the groups in flight keep their Q, dO, K, V and
-    // dQ-accumulator rows (~1.5 KB per row) in L2; deterministic mode:
-    // key-block-major over all heads.
+    // producer_role).  Units are claimed dynamically for packed sequences
+    // (lengths vary without a pattern) and in the deterministic mode;
+    // otherwise CTA c takes units c, c + grid, ..., which measured faster on
+    // dense inputs even under a causal mask (causal S = 1024 / 2048: 567 /
+    // 770 TFLOPS static against 469 / 617 claimed), given the longest-first
+    // order below.  Dense order: head-major
+    // (g = 1) without a causal mask; with one, longest first within groups
+    // of heads (causal S = 4096: 748 -> 846 TFLOPS), the group sized so that
+    // the groups in flight keep their Q, dO, K, V and dQ-accumulator rows
+    // (~1.5 KB per row) in L2; deterministic mode: key-block-major over all
+    // heads.
     {
       const long long bh = (long long)B * Hkv;
-      const bool dynamic = packed || deterministic || (causal && Sk <= 2048);
+      const bool dynamic = packed || deterministic;
       long long g = 1;
       if (deterministic) g = bh;
-      else if (dynamic && causal) g = (64ll << 20) / ((long long)Sk * 1536);
+      else if (causal) g = (64ll << 20) / ((long long)Sk * 1536);
       if (g < 1) g = 1;
       if (g > 16 && !deterministic) g = 16;
       if (g > bh) g = bh;
