@@ -16,7 +16,15 @@
 namespace fa {
 namespace {
 
-constexpr int kDefaultEmuPer16 = 0;
+// -1: chosen per configuration by default_emu_per_16().
+constexpr int kDefaultEmuPer16 = -1;
+
+// Share of the softmax exponentials computed by the FMA-pipe polynomial
+// (of every 16) when the caller leaves it to the library: measured on GB300
+// (B=8, S=4096, forward TFLOPS for 0 / 2 / 3 / 4 of 16): D=128 causal
+// 1126 / 1158 / 1116 / 1116; D=128 non-causal 1403 / 1369 / 1355 / 1356;
+// D=64 non-causal 814 / 810 / 677 / 677 and causal 668 / 665 / 606 / 607.
+int default_emu_per_16(int D, int causal) { return (D == 128 && causal) ? 2 : 0; }
 constexpr float kDefaultThreshold = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -176,7 +184,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
     L.p.wait_limit_ns = kDefaultWaitLimitNs;
     L.D = D;
     L.causal = causal != 0;
-    L.emu_per_16 = tune.emu_per_16;
+    L.emu_per_16 = tune.emu_per_16 >= 0 ? tune.emu_per_16 : default_emu_per_16(D, causal);
     L.num_sms = num_sms;
     return launch_fwd(L, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {

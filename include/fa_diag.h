@@ -33,7 +33,9 @@ typedef struct {
   int emu_per_16;
 } fa_fwd_tuning;
 
-/* The defaults fa_fwd() uses. */
+/* The defaults fa_fwd() uses.  emu_per_16 is -1 there: the library picks
+ * per configuration (2 of 16 for causal D = 128, where it measured 3% faster
+ * on GB300; 0 otherwise). */
 FA_API fa_fwd_tuning fa_fwd_default_tuning(void);
 
 /* fa_fwd() with explicit knobs; `t` may be NULL for the defaults. */

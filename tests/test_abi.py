@@ -70,7 +70,7 @@ def test_forward_rejects_bad_arguments(lib, kw, status):
 def test_forward_tuning_validation(lib):
     from exact_attention_78_gb300.binding import FwdTuning
     t = lib.fa_fwd_default_tuning()
-    assert t.rescale_threshold == 8.0 and t.emu_per_16 in (0, 2, 3, 4)
+    assert t.rescale_threshold == 8.0 and t.emu_per_16 in (-1, 0, 2, 3, 4)
     for thr, emu in ((-1.0, 0), (17.0, 0), (8.0, 1), (8.0, 5), (float("nan"), 0)):
         bad = FwdTuning(thr, emu)
         assert lib.fa_fwd_ex(A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, 0.125, None, ctypes.byref(bad), None) == 1

@@ -83,10 +83,13 @@ def test_causal_first_row_equals_first_value(fa):
 def test_lazy_equals_eager_under_stress(fa, causal):
     """Q x 4 (logit std ~16): running maxima keep growing.  Lazy (threshold 8)
     and eager (threshold 0) rescaling agree up to rounding, and both match
-    the oracle."""
+    the oracle.  Both runs use the hardware exponential only, so that the
+    comparison isolates the rescaling rule (the FMA polynomial's own error
+    depends on its argument, which differs between the two rules; its
+    accuracy has its own tests)."""
     q, k, v = _dense(1, 4, 4, 1024, 1024, 128, seed=1, q_scale=4.0)
-    o_l, lse_l = _run(fa, q, k, v, causal, rescale_threshold=8.0)
-    o_e, lse_e = _run(fa, q, k, v, causal, rescale_threshold=0.0)
+    o_l, lse_l = _run(fa, q, k, v, causal, rescale_threshold=8.0, emu_per_16=0)
+    o_e, lse_e = _run(fa, q, k, v, causal, rescale_threshold=0.0, emu_per_16=0)
     check_forward_full(o_l, lse_l, q, k, v, causal, 128 ** -0.5)
     check_forward_full(o_e, lse_e, q, k, v, causal, 128 ** -0.5)
     assert float((o_l.float() - o_e.float()).abs().max()) <= 1.6e-2
