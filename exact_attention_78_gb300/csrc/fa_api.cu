@@ -200,7 +200,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, const int* cu_seqlens_host,
                              int total_q, int deterministic) {
   if (deterministic != 0 && deterministic != 1) return 0;
-  if (D != 128 || total_q < 0) return 0;
+  if ((D != 64 && D != 128) || total_q < 0) return 0;
   const bool packed = cu_seqlens_host != nullptr || total_q > 0;
   if (!packed) {
     if (check_shapes(B, Hq, Hkv, Sq, Sk, D, 1.0f, nullptr) != FA_OK) return 0;
@@ -244,9 +244,10 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
     fa_status st = check_shapes(B, Hq, Hkv, Sq, Sk, D, scale, cu_seqlens);
     if (st != FA_OK) return st;
-    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
     const bool packed = cu_seqlens != nullptr;
-    if (packed && tune.paired == 1) return FA_ERR_UNSUPPORTED;   // the paired kernel is dense only
+    // the paired kernel is for the dense layout at D = 128 only
+    if ((packed || D != 128) && tune.paired == 1) return FA_ERR_UNSUPPORTED;
     const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Sq, D, deterministic, packed);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < ws.total)
       return FA_ERR_WORKSPACE;
@@ -309,7 +310,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.scale_log2 = scale * kLog2e;
     L.p.wait_limit_ns = kDefaultWaitLimitNs;
     L.num_sms = num_sms;
-    L.pair = tune.paired == 1 && !packed;
+    L.pair = tune.paired == 1 && !packed && D == 128;
     return launch_bwd(L, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {
     return FA_ERR_CUDA;

@@ -61,7 +61,6 @@ namespace bwd {
 
 __device__ DeviceError g_err;
 
-constexpr int kD = 128;        // head dimension of this kernel
 constexpr int kBN = 128;       // keys per work unit
 constexpr int kBM = 64;        // query rows per step
 constexpr int kThreads = 512;
@@ -75,10 +74,13 @@ constexpr int kRingReaders = 128 + 128 + 128 + 32 + 1;
 enum Site { kSiteEsS = 1, kSiteEsQ, kSiteEsDs, kSiteDqFull, kSiteDqTicket, kSiteAcc, kSiteMmaKV, kSiteMmaQ,
             kSiteMmaP, kSiteMmaDq, kSiteMmaAcc, kSiteProdKV, kSiteProdQ };
 
+// Shared-memory layout for head dimension kD (64 or 128): tiles of kD / 64
+// chunks, each 64 features (128 bytes) wide.
+template <int kD>
 struct Layout {
-  static constexpr int kKTile = kBN * kD * 2;        // 32 KB, 2 chunks of 128 rows x 128 B
+  static constexpr int kKTile = kBN * kD * 2;        // kD = 128: 32 KB, 2 chunks of 128 rows x 128 B
   static constexpr int kKChunk = kBN * 128;          // 16 KB
-  static constexpr int kQTile = kBM * kD * 2;        // 16 KB, 2 chunks of 64 rows x 128 B
+  static constexpr int kQTile = kBM * kD * 2;        // kD = 128: 16 KB, 2 chunks of 64 rows x 128 B
   static constexpr int kQChunk = kBM * 128;          // 8 KB
   static constexpr int kStageStride = 2 * kQTile;                 // Q, dO (1024-aligned)
   static constexpr int kRowTermBytes = 2 * kBM * 4;               // -LSE2, -Delta of the stage's rows
@@ -103,10 +105,31 @@ struct Layout {
 
 // ------------------------------------------------------------- pre / post --
 
+// This lane's kD / 32 consecutive elements of a row: sum of dO * O, and the
+// same elements of the FP32 dQ accumulator set to zero.
+template <int kD>
+FA_DEV float row_dot(const __nv_bfloat16* o, const __nv_bfloat16* g) {
+  float acc = 0.0f;
+#pragma unroll
+  for (int e = 0; e < kD / 64; ++e) {
+    const float2 a = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(o)[e]);
+    const float2 b = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(g)[e]);
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
+  }
+  return acc;
+}
+template <int kD>
+FA_DEV void zero_row_part(float* a) {
+  if constexpr (kD == 128) *reinterpret_cast<float4*>(a) = make_float4(0.f, 0.f, 0.f, 0.f);
+  else *reinterpret_cast<float2*>(a) = make_float2(0.f, 0.f);
+}
+
 // One warp per padded query row (b, h, q): stores -LSE * log2(e) and -Delta
 // (negated so the main kernel adds them with one packed FMA / ADD) and zeroes
 // the row's dQ accumulator.  Rows q >= Sq (padding) and rows that saw no key
 // (LSE = -inf) get -inf and 0, so their weights come out as exactly 0.
+template <int kD>
 __global__ void pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                            const float* __restrict__ lse, float* __restrict__ ndelta, float* __restrict__ nlse2,
                            float* __restrict__ dq_acc, int* __restrict__ tickets, long long n_tickets,
@@ -123,24 +146,15 @@ __global__ void pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloa
     const int b = (int)(bh / Hq);
     float dl = 0.0f, l2 = -INFINITY;
     if (q < Sq) {
-      const size_t off = ((size_t(b) * Sq + q) * Hq + h) * kD + lane * 4;
-      const uint2 ov = *reinterpret_cast<const uint2*>(o + off);
-      const uint2 gv = *reinterpret_cast<const uint2*>(dout + off);
-      const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
-      float acc = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float2 a = __bfloat1622float2(op[e]), g = __bfloat1622float2(gp[e]);
-        acc = fmaf(a.x, g.x, acc);
-        acc = fmaf(a.y, g.y, acc);
-      }
+      const size_t off = ((size_t(b) * Sq + q) * Hq + h) * kD + lane * (kD / 32);
+      const float acc0 = row_dot<kD>(o + off, dout + off);
+      float acc = acc0;
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
       dl = -acc;
       const float lv = lse[(size_t(b) * Hq + h) * Sq + q];
       l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
-      *reinterpret_cast<float4*>(dq_acc + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+      zero_row_part<kD>(dq_acc + off);
     }
     if (lane == 0) {
       ndelta[r] = dl;
@@ -226,6 +240,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ cu, 
 // rows of all sequences (sequence b from plan[B+1+b], rounded up to 64 rows);
 // padding rows get -inf and 0 so their weights are exactly 0.  One warp per
 // padded row; the real rows' dQ accumulator rows are zeroed.
+template <int kD>
 __global__ void pre_packed_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                   const float* __restrict__ lse, const int* __restrict__ cu,
                                   const int* __restrict__ plan, float* __restrict__ ndelta,
@@ -253,24 +268,14 @@ __global__ void pre_packed_kernel(const __nv_bfloat16* __restrict__ o, const __n
       const int off = pr - pad[lo];
       if (off < cu[lo + 1] - cu[lo]) {
         const int tok = cu[lo] + off;
-        const size_t e = ((size_t)tok * Hq + h) * kD + lane * 4;
-        const uint2 ov = *reinterpret_cast<const uint2*>(o + e);
-        const uint2 gv = *reinterpret_cast<const uint2*>(dout + e);
-        const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
-        float acc = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float2 a = __bfloat1622float2(op[k]), g = __bfloat1622float2(gp[k]);
-          acc = fmaf(a.x, g.x, acc);
-          acc = fmaf(a.y, g.y, acc);
-        }
+        const size_t e = ((size_t)tok * Hq + h) * kD + lane * (kD / 32);
+        float acc = row_dot<kD>(o + e, dout + e);
 #pragma unroll
         for (int sft = 16; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
         dl = -acc;
         const float lv = lse[(size_t)h * total + tok];
         l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
-        *reinterpret_cast<float4*>(dq_acc + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        zero_row_part<kD>(dq_acc + e);
       }
     }
     if (lane == 0) {
@@ -375,8 +380,9 @@ __device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p) {
   return w;
 }
 
+template <int kD>
 struct Shared {
-  using L = Layout;
+  using L = Layout<kD>;
   uint8_t* base;
   uint32_t sbase;
   FA_DEV uint32_t bar(int i) const { return sbase + L::kBars + 8 * i; }
@@ -426,8 +432,8 @@ constexpr uint32_t kColBuf = 128, kColDPoff = 64, kColDV = 256, kColDK = 384;
 // producer claims units from a counter in global memory (atomicAdd, so SMs
 // that finish early take more) and announces them, in claim order, through
 // a small ring in shared memory that every other role reads.  -1 ends it.
-template <bool DYN>
-FA_DEV int next_unit(const Shared& sh, int k, const BwdParams& p, int site, int total_units) {
+template <int kD, bool DYN>
+FA_DEV int next_unit(const Shared<kD>& sh, int k, const BwdParams& p, int site, int total_units) {
   if constexpr (!DYN) {
     const int u = (int)blockIdx.x + k * (int)gridDim.x;
     return u < total_units ? u : -1;
@@ -439,8 +445,8 @@ FA_DEV int next_unit(const Shared& sh, int k, const BwdParams& p, int site, int 
   return u;
 }
 
-template <bool PACKED, bool DYN>
-__device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUtensorMap* tk,
+template <int kD, bool PACKED, bool DYN>
+__device__ void producer_role(const Shared<kD>& sh, const CUtensorMap* tq, const CUtensorMap* tk,
                               const CUtensorMap* tv, const CUtensorMap* tdo, const BwdParams& p,
                               const int total_units) {
   uint32_t sit = 0, ukv = 0;
@@ -463,12 +469,12 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
     const Unit w = decode_unit<PACKED>(u, p);
     if (w.steps == 0) continue;
     if (!mbar_wait_bounded(sh.kv_empty(), (ukv & 1) ^ 1, sh.abort(), &g_err, kSiteProdKV, p.wait_limit_ns)) return;
-    mbar_arrive_expect_tx(sh.kv_full(), 2 * Layout::kKTile);
+    mbar_arrive_expect_tx(sh.kv_full(), 2 * Layout<kD>::kKTile);
     const int krow = u_kbase<PACKED>(w, p) + kBN * w.n;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      tma_load_3d(sh.sbase + Layout::kK + c * Layout::kKChunk, tk, sh.kv_full(), c * 64, w.hk, krow);
-      tma_load_3d(sh.sbase + Layout::kV + c * Layout::kKChunk, tv, sh.kv_full(), c * 64, w.hk, krow);
+    for (int c = 0; c < kD / 64; ++c) {
+      tma_load_3d(sh.sbase + Layout<kD>::kK + c * Layout<kD>::kKChunk, tk, sh.kv_full(), c * 64, w.hk, krow);
+      tma_load_3d(sh.sbase + Layout<kD>::kV + c * Layout<kD>::kKChunk, tv, sh.kv_full(), c * 64, w.hk, krow);
     }
     for (int s = 0; s < w.steps; ++s, ++sit) {
       const int h = w.hk * p.group + s / w.nq;
@@ -479,15 +485,15 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
         return;
       // Q on its own barrier (the S^T product needs nothing else), then dO
       // and the row terms
-      mbar_arrive_expect_tx(sh.q_full(st), Layout::kQTile);
-      mbar_arrive_expect_tx(sh.qd_full(st), Layout::kQTile + 2 * kBM * 4);
+      mbar_arrive_expect_tx(sh.q_full(st), Layout<kD>::kQTile);
+      mbar_arrive_expect_tx(sh.qd_full(st), Layout<kD>::kQTile + 2 * kBM * 4);
       const int qrow = u_qbase<PACKED>(w, p) + kBM * i;
       const uint32_t sb = sh.stage(st);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) tma_load_3d(sb + c * Layout::kQChunk, tq, sh.q_full(st), c * 64, h, qrow);
+      for (int c = 0; c < kD / 64; ++c) tma_load_3d(sb + c * Layout<kD>::kQChunk, tq, sh.q_full(st), c * 64, h, qrow);
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-        tma_load_3d(sb + Layout::kQTile + c * Layout::kQChunk, tdo, sh.qd_full(st), c * 64, h, qrow);
+      for (int c = 0; c < kD / 64; ++c)
+        tma_load_3d(sb + Layout<kD>::kQTile + c * Layout<kD>::kQChunk, tdo, sh.qd_full(st), c * 64, h, qrow);
       const size_t roff = u_rt<PACKED>(w, p) + size_t(h) * p.sq_pad + size_t(kBM) * i;
       bulk_load(sh.row_terms(st), p.nlse2 + roff, kBM * 4, sh.qd_full(st));
       bulk_load(sh.row_terms(st) + kBM * 4, p.ndelta + roff, kBM * 4, sh.qd_full(st));
@@ -498,13 +504,13 @@ __device__ void producer_role(const Shared& sh, const CUtensorMap* tq, const CUt
 
 // Unrolled K steps (K = D in 16-wide steps) of S^T = K Q^T or dP^T = V dO^T;
 // both operands K-major: step kk reads 64-wide chunk kk/4 at byte 32*(kk%4).
-template <int KK>
+template <int kD, int KK>
 FA_DEV void score_steps(uint32_t d, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi, uint32_t idesc) {
   if constexpr (KK < kD / 16) {
-    constexpr uint32_t oa = ((KK >> 2) * Layout::kKChunk + (KK & 3) * 32) >> 4;
-    constexpr uint32_t ob = ((KK >> 2) * Layout::kQChunk + (KK & 3) * 32) >> 4;
+    constexpr uint32_t oa = ((KK >> 2) * Layout<kD>::kKChunk + (KK & 3) * 32) >> 4;
+    constexpr uint32_t ob = ((KK >> 2) * Layout<kD>::kQChunk + (KK & 3) * 32) >> 4;
     mma_ss_w<oa, ob>(d, alo, ahi, blo, bhi, idesc, KK > 0 ? 1u : 0u);
-    score_steps<KK + 1>(d, alo, ahi, blo, bhi, idesc);
+    score_steps<kD, KK + 1>(d, alo, ahi, blo, bhi, idesc);
   }
 }
 // Unrolled K steps (64 queries in 16-wide steps) of dV += P^T dO and
@@ -532,14 +538,16 @@ FA_DEV void dq_steps(uint32_t d_dq, uint32_t klo, uint32_t khi, uint32_t slo, ui
 }
 
 // MMA issuer: the whole warp runs this, converged; an elected lane issues.
-template <bool PACKED, bool DYN>
-__device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
+template <int kD, bool PACKED, bool DYN>
+__device__ void mma_role(const Shared<kD>& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   constexpr uint32_t kIdS = idesc_bf16_f32(kBN, kBM, false, false);   // S^T, dP^T: 128 keys x 64 queries
   constexpr uint32_t kIdG = idesc_bf16_f32(kBN, kD, false, true);     // dV, dK: A in TMEM, B MN-major
-  constexpr uint32_t kIdQ = idesc_bf16_f32(kD, kBM, true, true);      // dQ^T: A = K^T, B = dS^T
-  const uint32_t kb = sh.sbase + Layout::kK, vb = sh.sbase + Layout::kV;
+  // dQ^T: A = K^T, B = dS^T; always M = 128 rows: with kD = 64 the second
+  // 64 rows read the next tile in shared memory (V) and are never used
+  constexpr uint32_t kIdQ = idesc_bf16_f32(128, kBM, true, true);
+  const uint32_t kb = sh.sbase + Layout<kD>::kK, vb = sh.sbase + Layout<kD>::kV;
   const uint64_t dk_kmaj = sdesc_sw128(kb, 16, 1024), dv_kmaj = sdesc_sw128(vb, 16, 1024);
-  const uint64_t dk_mn = sdesc_sw128(kb, Layout::kKChunk, 1024);
+  const uint64_t dk_mn = sdesc_sw128(kb, Layout<kD>::kKChunk, 1024);
   uint32_t sit = 0, ukv = 0;
 
   auto wait = [&](uint32_t bar, uint32_t parity, int site) -> bool {
@@ -558,18 +566,18 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
     if (!wait(sh.q_full(st), ph, kSiteMmaQ)) return false;
     if (p.deterministic && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
     const uint64_t dq = sdesc_sw128(sh.stage(st), 16, 1024);
-    score_steps<0>(tmem + kColBuf * buf, desc_lo(dk_kmaj), desc_hi(dk_kmaj), desc_lo(dq), desc_hi(dq), kIdS);
+    score_steps<kD, 0>(tmem + kColBuf * buf, desc_lo(dk_kmaj), desc_hi(dk_kmaj), desc_lo(dq), desc_hi(dq), kIdS);
     if (!p.deterministic && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
     if (!wait(sh.qd_full(st), ph, kSiteMmaQ)) return false;
-    const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout::kQTile, 16, 1024);
-    score_steps<0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dv_kmaj), desc_hi(dv_kmaj), desc_lo(dg), desc_hi(dg),
+    const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout<kD>::kQTile, 16, 1024);
+    score_steps<kD, 0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dv_kmaj), desc_hi(dv_kmaj), desc_lo(dg), desc_hi(dg),
                    kIdS);
     mma_commit_w(sh.s_full(buf));
     return true;
   };
 
   for (int k = 0;; ++k) {
-    const int u = next_unit<DYN>(sh, k, p, kSiteMmaKV, total_units);
+    const int u = next_unit<kD, DYN>(sh, k, p, kSiteMmaKV, total_units);
     if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     if (w.steps == 0) continue;
@@ -584,15 +592,15 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
       if (s == 0 && ukv > 0 && !wait(sh.acc_empty(), (ukv - 1) & 1, kSiteMmaAcc)) return;
       // dV += P^T dO_i, dK += dS^T Q_i (B MN-major: D contiguous, 64-wide
       // chunks 8 KB apart)
-      const uint64_t dgo = sdesc_sw128(sh.stage(st) + Layout::kQTile, Layout::kQChunk, 1024);
-      const uint64_t dqq = sdesc_sw128(sh.stage(st), Layout::kQChunk, 1024);
+      const uint64_t dgo = sdesc_sw128(sh.stage(st) + Layout<kD>::kQTile, Layout<kD>::kQChunk, 1024);
+      const uint64_t dqq = sdesc_sw128(sh.stage(st), Layout<kD>::kQChunk, 1024);
       grad_steps<0>(tmem + kColDV, tmem + kColDK, tmem + kColBuf * buf, tmem + kColBuf * buf + kColDPoff,
                     desc_lo(dgo), desc_hi(dgo), desc_lo(dqq), desc_hi(dqq), kIdG, s > 0 ? 1u : 0u);
       mma_commit_w(sh.qd_empty(st));
       // dQ_i^T = K^T dS^T over the dP^T columns of this buffer (its dS^T has
       // just been read by the dK product, issued before): M = D (K MN-major,
       // chunks 16 KB apart), N = 64 queries (dS^T MN-major), K = 128 keys
-      const uint64_t dsd = sdesc_sw128(sh.ds(buf), Layout::kDsBytes, 1024);
+      const uint64_t dsd = sdesc_sw128(sh.ds(buf), Layout<kD>::kDsBytes, 1024);
       dq_steps<0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd),
                   kIdQ);
       mma_commit_w(sh.dq_full(buf));
@@ -607,8 +615,8 @@ __device__ void mma_role(const Shared& sh, const uint32_t tmem, const BwdParams&
 // P / dS warpgroups: thread = key row kr of the unit's key block; warpgroup
 // H handles query columns [32 H, 32 H + 32) of each 64-row step, so two
 // warpgroups (one warp per scheduler each) share the elementwise work.
-template <bool PACKED, bool DYN, int H>
-__device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const BwdParams& p,
+template <int kD, bool PACKED, bool DYN, int H>
+__device__ void elementwise_role(const Shared<kD>& sh, const uint32_t tmem, const BwdParams& p,
                                  const int total_units) {
   constexpr int kC0 = 32 * H;   // first query column of this warpgroup
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -618,7 +626,7 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
   const uint64_t sl2x2 = pk2(sl2, sl2);
   uint32_t sit = 0;
   for (int k = 0;; ++k) {
-    const int u = next_unit<DYN>(sh, k, p, kSiteEsQ, total_units);
+    const int u = next_unit<kD, DYN>(sh, k, p, kSiteEsQ, total_units);
     if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     const int key = kBN * w.n + kr;
@@ -688,8 +696,8 @@ __device__ void elementwise_role(const Shared& sh, const uint32_t tmem, const Bw
 // two row-major FP32 staging tiles in shared memory (queries 0-31 and 32-63
 // of the block, 32 x 128 each); the reduce issuer adds each into the FP32
 // accumulator.  At the end of a unit it writes dK (scaled) and dV.
-template <bool PACKED, bool DYN>
-__device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
+template <int kD, bool PACKED, bool DYN>
+__device__ void dq_role(const Shared<kD>& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
   const int d = wq * 32 + lane;           // dQ^T lane = feature; dK/dV lane = key row
@@ -698,7 +706,7 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
   __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk);
   __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv);
   for (int k = 0;; ++k) {
-    const int u = next_unit<DYN>(sh, k, p, kSiteDqFull, total_units);
+    const int u = next_unit<kD, DYN>(sh, k, p, kSiteDqFull, total_units);
     if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     bool stop = false;
@@ -727,7 +735,8 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
         }
         float* stage = sh.dq_stage(half);
 #pragma unroll
-        for (int c = 0; c < kDqRows; ++c) stage[c * kD + d] = __uint_as_float(v[half][c]);
+        for (int c = 0; c < kDqRows; ++c)
+          if (d < kD) stage[c * kD + d] = __uint_as_float(v[half][c]);   // lanes >= kD: padding rows
         fence_proxy_async_smem();
         mbar_arrive(sh.dqs_full(half));
       }
@@ -793,8 +802,8 @@ __device__ void dq_role(const Shared& sh, const uint32_t tmem, const BwdParams& 
 // completion latency of the additions is not paid per step.  Waits point
 // only from key block n to block n - 1 of the same head, and no ticket is
 // held across units (heads), so the waits cannot form a cycle.
-template <bool PACKED, bool DYN>
-__device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
+template <int kD, bool PACKED, bool DYN>
+__device__ void reduce_role(const Shared<kD>& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
   uint32_t sit = 0;
   bool pending1 = false;   // tile 1 of the previous step is still being read
   int* held = nullptr;     // deterministic mode: ticket of the previous step, not yet released
@@ -805,7 +814,7 @@ __device__ void reduce_role(const Shared& sh, const CUtensorMap* tdq, const BwdP
     held = nullptr;
   };
   for (int k = 0;; ++k) {
-    const int u = next_unit<DYN>(sh, k, p, kSiteDqFull, total_units);
+    const int u = next_unit<kD, DYN>(sh, k, p, kSiteDqFull, total_units);
     if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     for (int s = 0; s < w.steps; ++s, ++sit) {
@@ -859,7 +868,7 @@ done:
   if (held) release_held();
 }
 
-template <bool PACKED, bool DYN>
+template <int kD, bool PACKED, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -867,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x / 32;
-  Shared sh;
+  Shared<kD> sh;
   sh.base = smem;
   sh.sbase = smem_u32(smem);
   if (threadIdx.x == 0) {
@@ -917,21 +926,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // register split (sums to the 512 x 128 the block was launched with)
   if (warp < 4) {
     reg_alloc<160>();
-    elementwise_role<PACKED, DYN, 0>(sh, tmem, p, total_units);
+    elementwise_role<kD, PACKED, DYN, 0>(sh, tmem, p, total_units);
   } else if (warp < 8) {
-    dq_role<PACKED, DYN>(sh, tmem, p, total_units);
+    dq_role<kD, PACKED, DYN>(sh, tmem, p, total_units);
   } else if (warp < 12) {
     reg_dealloc<64>();
     if (warp == 8) {
-      if ((threadIdx.x % 32) == 0) producer_role<PACKED, DYN>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
+      if ((threadIdx.x % 32) == 0) producer_role<kD, PACKED, DYN>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
     } else if (warp == 9) {
-      mma_role<PACKED, DYN>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
+      mma_role<kD, PACKED, DYN>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
     } else if (warp == 10) {
-      if ((threadIdx.x % 32) == 0) reduce_role<PACKED, DYN>(sh, &tm_dqacc, p, total_units);
+      if ((threadIdx.x % 32) == 0) reduce_role<kD, PACKED, DYN>(sh, &tm_dqacc, p, total_units);
     }
   } else {
     reg_alloc<160>();
-    elementwise_role<PACKED, DYN, 1>(sh, tmem, p, total_units);
+    elementwise_role<kD, PACKED, DYN, 1>(sh, tmem, p, total_units);
   }
   if (ld_shared_volatile(sh.abort())) {
     const uint64_t t0 = globaltimer_ns();
@@ -947,9 +956,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace bwd
 
-fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
+namespace {
+
+template <int kD>
+fa_status launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   const BwdParams& p = L.p;
-  if (p.D != bwd::kD) return FA_ERR_UNSUPPORTED;
   const bool packed = p.cu_seqlens != nullptr;
   // rows of the [rows, H, D] arrays
   const int rows_q = packed ? p.Sq : p.B * p.Sq;
@@ -966,18 +977,18 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   if (pre_blocks < 1) pre_blocks = 1;
   if (packed) {
     bwd::plan_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.Sq, p.plan);
-    bwd::pre_packed_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
+    bwd::pre_packed_kernel<kD><<<(unsigned)pre_blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
         p.cu_seqlens, p.plan, p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq,
         p.sq_pad);
   } else {
-    bwd::pre_kernel<<<(unsigned)pre_blocks, 256, 0, stream>>>(
+    bwd::pre_kernel<kD><<<(unsigned)pre_blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
         p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq, p.sq_pad);
   }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
-  if (L.pair && !packed) {
+  if (L.pair && !packed && kD == 128) {
     if ((st = launch_bwd_pair_main(L, stream)) != FA_OK) return st;
   } else {
     CUtensorMap tq, tk, tv, tdo, tdq;
@@ -989,12 +1000,12 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
     if ((st = make_tmap_rows_heads_d(&tv, L.v, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
     static bool attr_done = false;
     if (!attr_done) {
-      if (cudaFuncSetAttribute(bwd::bwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               bwd::Layout::kDynamic) != cudaSuccess ||
-          cudaFuncSetAttribute(bwd::bwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               bwd::Layout::kDynamic) != cudaSuccess ||
-          cudaFuncSetAttribute(bwd::bwd_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               bwd::Layout::kDynamic) != cudaSuccess)
+      if (cudaFuncSetAttribute(bwd::bwd_kernel<kD, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bwd::Layout<kD>::kDynamic) != cudaSuccess ||
+          cudaFuncSetAttribute(bwd::bwd_kernel<kD, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bwd::Layout<kD>::kDynamic) != cudaSuccess ||
+          cudaFuncSetAttribute(bwd::bwd_kernel<kD, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bwd::Layout<kD>::kDynamic) != cudaSuccess)
         return FA_ERR_CUDA;
       attr_done = true;
     }
@@ -1006,11 +1017,11 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
     // packed layouts always use the dynamic schedule (their units differ in
     // length); dense ones as chosen by the caller (sched_dynamic)
     if (packed)
-      bwd::bwd_kernel<true, true><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+      bwd::bwd_kernel<kD, true, true><<<grid, bwd::kThreads, bwd::Layout<kD>::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
     else if (p.sched_dynamic)
-      bwd::bwd_kernel<false, true><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
+      bwd::bwd_kernel<kD, false, true><<<grid, bwd::kThreads, bwd::Layout<kD>::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
     else
-      bwd::bwd_kernel<false, false><<<grid, bwd::kThreads, bwd::Layout::kDynamic, stream>>>(tq, tk, tv, tdo, tdq,
+      bwd::bwd_kernel<kD, false, false><<<grid, bwd::kThreads, bwd::Layout<kD>::kDynamic, stream>>>(tq, tk, tv, tdo, tdq,
                                                                                           p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
@@ -1022,6 +1033,14 @@ fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
   bwd::post_kernel<<<(unsigned)post_blocks, 256, 0, stream>>>(p.dq_acc, reinterpret_cast<__nv_bfloat16*>(p.dq),
                                                               n8, p.scale, packed ? p.plan + 2 * p.B + 3 : nullptr);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
+  if (L.p.D == 128) return launch_bwd_d<128>(L, stream);
+  if (L.p.D == 64) return launch_bwd_d<64>(L, stream);
+  return FA_ERR_UNSUPPORTED;
 }
 
 fa_status bwd_take_device_error() {

@@ -102,7 +102,7 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
  *   does not depend on the individual lengths: FP32 accumulator [total, Hq, D],
  *   row terms over each sequence's rows rounded up to 64 (Hq x (total rounded
  *   up to 64 + 64 B) each), the per-sequence offset tables and the tickets.
- * Returns 0 for arguments fa_bwd() would reject (including D != 128).
+ * Returns 0 for arguments fa_bwd() would reject.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, const int* cu_seqlens_host,
                                     int total_q, int deterministic);
@@ -118,7 +118,7 @@ FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int 
  *                  fa_bwd_workspace_size(...) bytes (for the packed layout
  *                  sized with total_q = Sq); contents on entry are ignored
  *                  and clobbered.
- * Head dimensions other than 128 are rejected with FA_ERR_UNSUPPORTED.
+ * Head dimension 64 or 128, like fa_fwd().
  * Launches three kernels on `stream` (row terms, main pass, dQ conversion),
  * four for the packed layout (a first one checks the offsets and builds the
  * per-sequence tables).

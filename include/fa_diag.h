@@ -68,6 +68,8 @@ FA_API fa_bwd_tuning fa_bwd_default_tuning(void);
 /* fa_bwd() with explicit knobs; `t` may be NULL for the defaults.  Same
  * arguments, workspace and errors as fa_bwd(); FA_ERR_INVALID_ARG if
  * t->paired is not -1, 0 or 1. */
+/* The paired kernel covers the dense layout at D = 128; paired = 1 with a
+ * packed layout or D = 64 returns FA_ERR_UNSUPPORTED. */
 FA_API fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
                            const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk,
                            int D, int causal, float scale, const int* cu_seqlens, int deterministic,

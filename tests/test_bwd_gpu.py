@@ -26,8 +26,8 @@ def fa():
     return fa_mod
 
 
-def _inputs(B, Hq, Hkv, Sq, Sk, seed=0, q_scale=1.0):
-    w = W.Workload("case", B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, D=128, causal=False, seed=seed, q_scale=q_scale)
+def _inputs(B, Hq, Hkv, Sq, Sk, seed=0, q_scale=1.0, D=128):
+    w = W.Workload("case", B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, D=D, causal=False, seed=seed, q_scale=q_scale)
     (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
     return q, k, v, do
 
@@ -41,7 +41,7 @@ def _gpu_grads(fa, q, k, v, do, causal, deterministic=False):
 
 
 def _check(grads, q, k, v, do, causal):
-    ref = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), causal, 128 ** -0.5)
+    ref = oracle.attention_backward(f64(q), f64(k), f64(v), f64(do), causal, q.shape[-1] ** -0.5)
     errs = []
     for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
         gg = f64(g)
@@ -105,6 +105,35 @@ def test_deterministic_is_bitwise_repeatable(fa, causal):
     c = _gpu_grads(fa, q, k, v, do, causal, deterministic=False)
     for x, y in zip(a, c):
         assert rel_fro(f64(x), f64(y)) <= 2e-3
+
+
+# ------------------------------------------------------------------ D = 64 --
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk", [
+    (1, 2, 2, 128, 128),
+    (2, 4, 2, 300, 300),     # grouped heads, ragged rows and keys
+    (1, 2, 1, 1000, 1000),   # several key blocks and query blocks
+    (1, 2, 2, 520, 300),     # Sq > Sk
+])
+def test_d64_shapes_full_compare(fa, causal, B, Hq, Hkv, Sq, Sk):
+    q, k, v, do = _inputs(B, Hq, Hkv, Sq, Sk, seed=12, D=64)
+    _check(_gpu_grads(fa, q, k, v, do, causal), q, k, v, do, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d64_deterministic_is_bitwise_repeatable(fa, causal):
+    q, k, v, do = _inputs(2, 4, 2, 700, 700, seed=13, D=64)
+    a = _gpu_grads(fa, q, k, v, do, causal, deterministic=True)
+    b = _gpu_grads(fa, q, k, v, do, causal, deterministic=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    _check(a, q, k, v, do, causal)
+
+
+def test_d64_stress_logits(fa):
+    q, k, v, do = _inputs(1, 2, 2, 512, 512, seed=1, q_scale=4.0, D=64)
+    _check(_gpu_grads(fa, q, k, v, do, True), q, k, v, do, True)
 
 
 # ---------------------------------------------------------------- full size --

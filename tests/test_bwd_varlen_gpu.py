@@ -24,13 +24,13 @@ def fa():
     return fa_mod
 
 
-def _packed(lens, Hq, Hkv, seed):
+def _packed(lens, Hq, Hkv, seed, D=128):
     cu = W.cu_seqlens_of(lens)
     T = int(cu[-1])
-    q = W.randn_bf16((T, Hq, 128), 100 * seed + 1)
-    k = W.randn_bf16((T, Hkv, 128), 100 * seed + 2)
-    v = W.randn_bf16((T, Hkv, 128), 100 * seed + 3)
-    do = W.randn_bf16((T, Hq, 128), 100 * seed + 4)
+    q = W.randn_bf16((T, Hq, D), 100 * seed + 1)
+    k = W.randn_bf16((T, Hkv, D), 100 * seed + 2)
+    v = W.randn_bf16((T, Hkv, D), 100 * seed + 3)
+    do = W.randn_bf16((T, Hq, D), 100 * seed + 4)
     return q, k, v, do, cu
 
 
@@ -46,7 +46,7 @@ def _reference(q, k, v, do, cu, causal, seqs=None, heads=None):
     """Per-sequence, per-head oracle gradients; dK/dV summed over each group."""
     Hq, Hkv = q.shape[1], k.shape[1]
     g = Hq // Hkv
-    scale = 128 ** -0.5
+    scale = q.shape[-1] ** -0.5
     out = {}
     seqs = range(len(cu) - 1) if seqs is None else seqs
     for b in seqs:
@@ -96,6 +96,12 @@ def _check_full(grads, q, k, v, do, cu, causal):
 ])
 def test_packed_backward_matches_oracle(fa, causal, lens, Hq, Hkv):
     q, k, v, do, cu = _packed(lens, Hq, Hkv, seed=len(lens))
+    _check_full(_gpu(fa, q, k, v, do, cu, causal), q, k, v, do, cu, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_backward_d64(fa, causal):
+    q, k, v, do, cu = _packed([1, 130, 0, 513, 256, 77], 4, 2, seed=9, D=64)
     _check_full(_gpu(fa, q, k, v, do, cu, causal), q, k, v, do, cu, causal)
 
 
