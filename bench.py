@@ -321,41 +321,75 @@ def run_gpu(args):
     ms_step = elapsed_ms / args.steps
     value = ws * flops_step / (ms_step * 1e-3) / 1e12
 
-    # end to end: pinned host inputs -> device -> fwd(+bwd) -> host outputs
+    # end to end through the public API: every step copies its own inputs in
+    # from pinned host memory and reads its own results (O, LSE and, with the
+    # backward, dQ, dK, dV) back to pinned host memory, all inside the timed
+    # region.  Two sets of device buffers and one stream per copy direction
+    # let step i + 1's inputs arrive, and step i - 1's results leave, while
+    # step i computes (the host link is full duplex).
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+        host_in = [t.pin_memory() for t in ((q, k, v, do) if have_bwd else (q, k, v))]
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         hg = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (qd, kd, vd)] if have_bwd else []
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hdo,) if have_bwd else ()))
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = ho.numel() * 2 + hl.numel() * 4 + sum(t.numel() * 2 for t in hg)
+        sets = []
+        for _ in range(2):
+            ins = [torch.empty_like(t) for t in ((qd, kd, vd, dod) if have_bwd else (qd, kd, vd))]
+            grads = [torch.empty_like(t) for t in (qd, kd, vd)] if have_bwd else []
+            sets.append((ins, torch.empty_like(o), torch.empty_like(lse), grads))
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        copied = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        read = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            qd.copy_(hq, non_blocking=True)
-            kd.copy_(hk, non_blocking=True)
-            vd.copy_(hv, non_blocking=True)
+        def e2e_issue(i):
+            bset = i % 2
+            ins, oo, ll, gg = sets[bset]
+            if i >= 2:
+                s_in.wait_event(computed[bset])      # step i - 2 has consumed this set's inputs
+            with torch.cuda.stream(s_in):
+                for dst, src in zip(ins, host_in):
+                    dst.copy_(src, non_blocking=True)
+                copied[bset].record(s_in)
+            stream.wait_event(copied[bset])
+            if i >= 2:
+                stream.wait_event(read[bset])        # step i - 2's results have left
+            fa.fwd(ins[0], ins[1], ins[2], causal=w.causal, cu_seqlens=cud, out=oo, lse=ll, emu_per_16=args.emu,
+                   stream=stream)
             if have_bwd:
-                dod.copy_(hdo, non_blocking=True)
-            step()
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
-            if have_bwd:
-                for hgt, g in zip(hg, (dq, dk, dv)):
+                fa.bwd(ins[0], ins[1], ins[2], oo, ll, ins[3], causal=w.causal, deterministic=det, workspace=ws_buf,
+                       dq=gg[0], dk=gg[1], dv=gg[2], paired=paired, cu_seqlens=cud, stream=stream)
+            computed[bset].record(stream)
+            s_out.wait_event(computed[bset])
+            with torch.cuda.stream(s_out):
+                ho.copy_(oo, non_blocking=True)
+                hl.copy_(ll, non_blocking=True)
+                for hgt, g in zip(hg, gg):
                     hgt.copy_(g, non_blocking=True)
+                read[bset].record(s_out)
 
-        e2e_step()
+        for i in range(2):
+            e2e_issue(i)
+        torch.cuda.synchronize()
         barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_e2e = max(3, args.steps // 4)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        for i in range(n_e2e):
+            e2e_issue(i)
+        stream.wait_stream(s_out)
+        stream.wait_stream(s_in)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = replicas.max_over_ranks(e0.elapsed_time(e1) / n_e2e, device="cuda")
         e2e = {"value": ws * flops_step / (e_ms * 1e-3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "pipeline": "double-buffered: next step's inputs in and previous step's results out during compute"}
 
     if rank != 0:
         replicas.finalize()
