@@ -127,6 +127,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+def code_only(src):
+    """Source text with comments and whitespace runs removed, so that a
+    comment edit does not retire a traffic record taken on the same code."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def measured_traffic(kernel, w):
     """DRAM bytes per launch of `kernel` from the committed ncu record, if it
     was taken on this workload and the kernel sources are unchanged since."""
@@ -144,8 +153,8 @@ def measured_traffic(kernel, w):
              "fwd_kernel": ["fa_fwd.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"]}[kernel]
     m = hashlib.sha256()
     for fn in files:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            m.update(f.read())
+        with open(os.path.join(csrc, fn)) as f:
+            m.update(code_only(f.read()).encode())
     if w.packed:
         return None
     want = "dense B=%d Hq=Hkv=%d S=%d D=%d %s" % (w.B, w.Hq, w.Sq, w.D, "causal" if w.causal else "non-causal")

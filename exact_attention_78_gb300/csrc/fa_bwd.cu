@@ -1,4 +1,5 @@
-// Backward pass of exact attention on sm_103a (dense layout, D = 128).
+// Backward pass of exact attention on sm_103a (dense and packed layouts,
+// head dimension D = 64 or 128).
 //
 // Three kernels per call:
 //   pre   Delta_i = sum_d dO_id * O_id and LSE_i * log2(e) per query row (FP32,
@@ -16,7 +17,7 @@
 //             dQ_i^T = K^T dS^T   -> added to the FP32 accumulator
 //         dK and dV stay in TMEM across the whole group and are written once
 //         per unit, so they need no atomics.  dQ partial sums are added by the
-//         TMA unit (bulk tensor reduce-adds of 32 x 128 FP32 tiles staged
+//         TMA unit (bulk tensor reduce-adds of 32 x D FP32 tiles staged
 //         through two shared-memory buffers, so one tile is written while the
 //         other is read), in deterministic mode in ascending key-block order
 //         enforced by one ticket per (batch, head, query block);
@@ -27,8 +28,15 @@
 // Blackwell's changed balance (the backward tile: five products, shared-memory
 // traffic the bottleneck), bullet "Paired-CTA backward pass" (dQ through global
 // atomic adds) and the paragraph on the deterministic backward mode and
-// longest-first ordering.  The paired-CTA (2-SM) MMA of that bullet is not
-// used here yet: every product runs on one SM's tensor core.
+// longest-first ordering.  Every product here runs on one SM's tensor core;
+// the paired-CTA (2-SM) variant of that bullet is the separate kernel in
+// fa_bwd_pair.cu.
+//
+// Schedules: a static one (CTA c takes units c, c + grid, ...) for dense
+// calls -- head-major without a mask, longest-first within L2-sized head
+// groups under a causal mask -- and a dynamic one (units claimed from an
+// atomic counter, announced to the roles through a ring in shared memory)
+// for packed and deterministic calls.
 //
 // Thread layout (512 threads, 16 warps, one CTA per SM; registers per thread
 // after setmaxnreg: elementwise 160, dQ 128, warps 8-11 64):
