@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--S", type=int, default=4096)
     ap.add_argument("--D", type=int, default=128)
     ap.add_argument("--emu", type=int, default=None, help="exp2 emulation: entries of every 16 on FMA")
+    ap.add_argument("--bwd-tune", default="",
+                    help="backward knobs as name=value,... (schedule, head_group, reverse_blocks, scores_first); "
+                         "default: the library's per-call choice")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline sample")
     return ap.parse_args()
@@ -263,6 +266,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     det = bool(w.extra.get("deterministic", args.deterministic))
     paired = True if args.paired else None
+    tuning = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.bwd_tune.split(",") if kv} or None
 
     have_bwd = not args.fwd_only
     ws_buf = dq = dk = dv = None
@@ -277,7 +281,7 @@ def run_gpu(args):
             dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
             fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, emu_per_16=args.emu)
             fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
-                   dv=dv, paired=paired, cu_seqlens=cud)
+                   dv=dv, paired=paired, cu_seqlens=cud, tuning=tuning)
         except fa.FAError as e:
             if e.status != 2:
                 raise
@@ -296,7 +300,7 @@ def run_gpu(args):
             ev_f1[i].record(stream)
         if have_bwd:
             fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
-                   dv=dv, paired=paired, cu_seqlens=cud)
+                   dv=dv, paired=paired, cu_seqlens=cud, tuning=tuning)
         if i is not None:
             ev_b1[i].record(stream)
 
@@ -370,7 +374,7 @@ def run_gpu(args):
                    stream=stream)
             if have_bwd:
                 fa.bwd(ins[0], ins[1], ins[2], oo, ll, ins[3], causal=w.causal, deterministic=det, workspace=ws_buf,
-                       dq=gg[0], dk=gg[1], dv=gg[2], paired=paired, cu_seqlens=cud, stream=stream)
+                       dq=gg[0], dk=gg[1], dv=gg[2], paired=paired, cu_seqlens=cud, stream=stream, tuning=tuning)
             computed[bset].record(stream)
             s_out.wait_event(computed[bset])
             with torch.cuda.stream(s_out):
@@ -427,6 +431,7 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w.describe(), "step": "fwd+bwd" if have_bwd else "fwd", "deterministic": det,
                    "bwd_kernel": "paired CTAs" if args.paired else "single CTA",
+                   **({"bwd_tuning": tuning} if tuning else {}),
                    "l2": "inputs larger than L2 (Q,K,V,O %d MiB each)" % (qd.numel() * 2 >> 20),
                    "parallelism": "replicas" if ws > 1 else "single"},
         "fwd_tflops": fwd_flops_of(w) / (fwd_ms * 1e-3) / 1e12,

@@ -28,7 +28,8 @@ class FwdTuning(ctypes.Structure):
 
 
 class BwdTuning(ctypes.Structure):
-    _fields_ = [("paired", ctypes.c_int)]
+    _fields_ = [("paired", ctypes.c_int), ("schedule", ctypes.c_int), ("head_group", ctypes.c_int),
+                ("reverse_blocks", ctypes.c_int), ("scores_first", ctypes.c_int)]
 
 
 _LIB = None
@@ -159,10 +160,15 @@ def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic=False, total_q=0, cu
 
 
 def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, workspace=None, dq=None, dk=None,
-        dv=None, paired=None, cu_seqlens=None, stream=None):
+        dv=None, paired=None, cu_seqlens=None, stream=None, tuning=None):
     """dQ, dK, dV of attention(q, k, v) given O, LSE and dO.  Dense [B,S,H,D]
     or packed [total,H,D] with cu_seqlens (LSE [Hq, total]).  paired=True runs
-    the main kernel on CTA pairs (paired tcgen05 MMAs; dense only)."""
+    the main kernel on CTA pairs (paired tcgen05 MMAs; dense only).  tuning:
+    a dict of fa_bwd_tuning fields (schedule, head_group, reverse_blocks,
+    scores_first) overriding the per-call defaults."""
+    unknown = set(tuning or {}) - {f[0] for f in BwdTuning._fields_}
+    if unknown:
+        raise KeyError("unknown backward tuning field(s): %s" % ", ".join(sorted(unknown)))
     lib = load_library()
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check_bf16(n, t)
@@ -178,11 +184,14 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, work
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq,
             Sk, D, int(bool(causal)), float(scale), _ptr(cu_seqlens), int(bool(deterministic)), _ptr(workspace),
             workspace.numel()]
-    if paired is None:
+    if paired is None and not tuning:
         st = lib.fa_bwd(*args, _stream(stream))
     else:
         t = lib.fa_bwd_default_tuning()
-        t.paired = int(bool(paired))
+        if paired is not None:
+            t.paired = int(bool(paired))
+        for name, val in (tuning or {}).items():
+            setattr(t, name, int(val))
         st = lib.fa_bwd_ex(*args, ctypes.byref(t), _stream(stream))
     _check(st, "fa_bwd")
     return dq, dk, dv

@@ -223,6 +223,10 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, cons
 fa_bwd_tuning fa_bwd_default_tuning(void) {
   fa_bwd_tuning t;
   t.paired = 0;
+  t.schedule = -1;
+  t.head_group = -1;
+  t.reverse_blocks = -1;
+  t.scores_first = -1;
   return t;
 }
 
@@ -233,8 +237,13 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   try {
     fa_bwd_tuning tune = fa_bwd_default_tuning();
     if (t) {
-      if (t->paired < -1 || t->paired > 1) return FA_ERR_INVALID_ARG;
+      if (t->paired > 1 || t->schedule > 1 || t->reverse_blocks > 1 || t->scores_first > 1 || t->head_group == 0)
+        return FA_ERR_INVALID_ARG;
       if (t->paired >= 0) tune.paired = t->paired;
+      tune.schedule = t->schedule;
+      tune.head_group = t->head_group;
+      tune.reverse_blocks = t->reverse_blocks;
+      tune.scores_first = t->scores_first;
     }
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
@@ -278,24 +287,32 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     // (lengths vary without a pattern) and in the deterministic mode;
     // otherwise CTA c takes units c, c + grid, ..., which measured faster on
     // dense inputs even under a causal mask (causal S = 1024 / 2048: 567 /
-    // 770 TFLOPS static against 469 / 617 claimed), given the longest-first
-    // order below.  Dense order: head-major
-    // (g = 1) without a causal mask; with one, longest first within groups
-    // of heads (causal S = 4096: 748 -> 846 TFLOPS), the group sized so that
-    // the groups in flight keep their Q, dO, K, V and dQ-accumulator rows
-    // (~1.5 KB per row) in L2; deterministic mode: key-block-major over all
-    // heads.
+    // 770 TFLOPS static against 469 / 617 claimed).  Dense order: head-major
+    // (g = 1) without a causal mask (all units equally long; a head's key
+    // blocks run together and share its Q / dO rows in L2).  With one,
+    // key-block-major within groups of g = 32 heads: the longest blocks start
+    // first, and each head has a few consecutive key blocks in flight, which
+    // move through the same query rows a few blocks apart (measured over
+    // g = 5 ... 512: 32 is within 2% of the best at S = 1K ... 32K, and
+    // causal S = 8192 B = 2 runs 914 -> 1018 TFLOPS against the former
+    // L2-footprint rule).  Deterministic mode: key-block-major over all
+    // heads, so that a block's predecessor in the ordered dQ additions was
+    // claimed as far ahead as possible, and each unit visits its query
+    // blocks last to first, so that it meets its predecessor's additions in
+    // the order they were made (causal S = 8192 B = 2: 607 -> 616 TFLOPS;
+    // packed varlen: 265 -> 317).
     {
       const long long bh = (long long)B * Hkv;
-      const bool dynamic = packed || deterministic;
+      const bool dynamic = tune.schedule >= 0 ? tune.schedule == 1 : (packed || deterministic);
       long long g = 1;
-      if (deterministic) g = bh;
-      else if (causal) g = (64ll << 20) / ((long long)Sk * 1536);
-      if (g < 1) g = 1;
-      if (g > 16 && !deterministic) g = 16;
+      if (tune.head_group > 0) g = tune.head_group;
+      else if (deterministic) g = bh;
+      else if (causal) g = 32;
       if (g > bh) g = bh;
       L.p.sched_group = (int)g;
       L.p.sched_dynamic = dynamic ? 1 : 0;
+      L.p.rev_blocks = tune.reverse_blocks >= 0 ? tune.reverse_blocks : (deterministic ? 1 : 0);
+      L.p.scores_first = tune.scores_first >= 0 ? tune.scores_first : (deterministic ? 0 : 1);
     }
     L.p.B = B;
     L.p.Hq = Hq;

@@ -231,6 +231,9 @@ FA_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.rea
 FA_DEV void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Wait until all committed bulk groups have completed (writes performed).
 FA_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's global-memory accesses made through the async proxy
+// (TMA, bulk copies and reductions) with its generic-proxy accesses.
+FA_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 FA_DEV void bulk_wait_group2() { asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); }
 
 FA_DEV void tma_prefetch_desc(const CUtensorMap* map) {

@@ -57,17 +57,41 @@ FA_API fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o,
  *           distributed shared memory (thousands of cycles of latency that
  *           the fully used tensor memory leaves no room to hide) and runs
  *           at 64 rows per SM.
+ * The other knobs apply to the unpaired kernel; negative selects the
+ * default, which depends on the call (layout, mask, deterministic mode).
+ *   schedule        dense layout: 0: CTA c of the persistent grid takes
+ *                   work units c, c + grid, ...; 1: each CTA claims its
+ *                   next unit from a counter in the workspace (packed
+ *                   layouts always claim).
+ *   head_group      dense layout: the unit order visits the key blocks of
+ *                   head_group (batch, kv head) pairs block by block (block
+ *                   0 of each pair, then block 1, ...), group after group;
+ *                   1 is head-major, a value >= B * Hkv key-block-major.
+ *                   Under a causal mask block 0 is the longest, so this is
+ *                   the longest-first order of "FlashAttention-4 ..." (the
+ *                   paragraph on longest-first scheduling), per group.
+ *   reverse_blocks  1: a unit visits its query blocks last to first.
+ *   scores_first    1: the next step's S^T product is issued before the
+ *                   MMA warp waits for the dQ read-out of its TMEM buffer;
+ *                   0: after.
+ * FA_ERR_INVALID_ARG for a value out of range (paired, schedule,
+ * reverse_blocks or scores_first > 1, head_group 0).
  */
 typedef struct {
   int paired;
+  int schedule;
+  int head_group;
+  int reverse_blocks;
+  int scores_first;
 } fa_bwd_tuning;
 
-/* The defaults fa_bwd() uses. */
+/* The defaults fa_bwd() uses: paired 0, every other knob -1 (chosen per
+ * call). */
 FA_API fa_bwd_tuning fa_bwd_default_tuning(void);
 
 /* fa_bwd() with explicit knobs; `t` may be NULL for the defaults.  Same
- * arguments, workspace and errors as fa_bwd(); FA_ERR_INVALID_ARG if
- * t->paired is not -1, 0 or 1. */
+ * arguments, workspace and errors as fa_bwd(), plus FA_ERR_INVALID_ARG for a
+ * knob out of range. */
 /* The paired kernel covers the dense layout at D = 128; paired = 1 with a
  * packed layout or D = 64 returns FA_ERR_UNSUPPORTED. */
 FA_API fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
