@@ -106,7 +106,7 @@ fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int row
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic, bool packed) {
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Hkv, int Sq, int D, int deterministic, bool packed) {
   BwdWorkspace w{};
   // row terms per head: dense, Sq rounded up to 64 per batch entry; packed,
   // every sequence rounded up to 64 rows, bounded by total + 64 per sequence
@@ -122,6 +122,10 @@ BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministi
   off = align256(off + heads_rt * sq_pad * sizeof(float));
   w.plan = off;
   if (packed) off = align256(off + (2 * size_t(B) + 4) * sizeof(int));
+  // packed: the unit order table, one entry per (key block, kv head); every
+  // sequence adds at most one partial key block
+  w.order = off;
+  if (packed) off = align256(off + (size_t(Sq) / 128 + size_t(B)) * size_t(Hkv) * sizeof(int2));
   w.sched = off;
   off = align256(off + sizeof(int));
   w.tickets = off;
@@ -204,7 +208,7 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, cons
   const bool packed = cu_seqlens_host != nullptr || total_q > 0;
   if (!packed) {
     if (check_shapes(B, Hq, Hkv, Sq, Sk, D, 1.0f, nullptr) != FA_OK) return 0;
-    return bwd_workspace_layout(B, Hq, Sq, D, deterministic, false).total;
+    return bwd_workspace_layout(B, Hq, Hkv, Sq, D, deterministic, false).total;
   }
   // packed: Sq = Sk = total_q rows (any 4-aligned non-null marker passes the
   // pointer checks of check_shapes; the offsets themselves are checked below)
@@ -217,7 +221,7 @@ size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, cons
       if (cu_seqlens_host[b + 1] < cu_seqlens_host[b] || cu_seqlens_host[b + 1] - cu_seqlens_host[b] > 262144)
         return 0;
   }
-  return bwd_workspace_layout(B, Hq, Sq, D, deterministic, true).total;
+  return bwd_workspace_layout(B, Hq, Hkv, Sq, D, deterministic, true).total;
 }
 
 fa_bwd_tuning fa_bwd_default_tuning(void) {
@@ -257,7 +261,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     const bool packed = cu_seqlens != nullptr;
     // the paired kernel is for the dense layout at D = 128 only
     if ((packed || D != 128) && tune.paired == 1) return FA_ERR_UNSUPPORTED;
-    const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Sq, D, deterministic, packed);
+    const BwdWorkspace ws = bwd_workspace_layout(B, Hq, Hkv, Sq, D, deterministic, packed);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < ws.total)
       return FA_ERR_WORKSPACE;
     int num_sms = 0;
@@ -281,6 +285,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.tickets = deterministic ? reinterpret_cast<int*>(wb + ws.tickets) : nullptr;
     L.p.cu_seqlens = cu_seqlens;
     L.p.plan = packed ? reinterpret_cast<int*>(wb + ws.plan) : nullptr;
+    L.p.order = packed ? reinterpret_cast<int2*>(wb + ws.order) : nullptr;
     L.p.sched = reinterpret_cast<int*>(wb + ws.sched);
     // Work schedule of the main kernel (see its decode_unit and
     // producer_role).  Units are claimed dynamically for packed sequences
@@ -301,11 +306,17 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     // blocks last to first, so that it meets its predecessor's additions in
     // the order they were made (causal S = 8192 B = 2: 607 -> 616 TFLOPS;
     // packed varlen: 265 -> 317).
+    // Packed layouts: (sequence, kv head) pairs sorted longest first, in
+    // groups of 16 pairs (deterministic: 32), key-block-major within a group
+    // (the plan kernel writes the order; varlen GQA workload, 64 sequences:
+    // groups of 8 / 16 / 32 / 64 / 512 pairs: 1013 / 1006 / 988 / 740 / 661
+    // TFLOPS, deterministic 591 / - / 717 / 632 / 569).
     {
       const long long bh = (long long)B * Hkv;
       const bool dynamic = tune.schedule >= 0 ? tune.schedule == 1 : (packed || deterministic);
       long long g = 1;
       if (tune.head_group > 0) g = tune.head_group;
+      else if (packed) g = deterministic ? 32 : 16;
       else if (deterministic) g = bh;
       else if (causal) g = 32;
       if (g > bh) g = bh;

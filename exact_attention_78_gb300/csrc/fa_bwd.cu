@@ -202,9 +202,23 @@ __global__ void post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __r
 // and tickets start), plan[2B+2] = the total number of key blocks (0 when
 // the offsets are invalid, so that nothing is computed) and plan[2B+3] = 1
 // for invalid offsets, which is also reported as FA_ERR_INVALID_ARG.
-__global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ cu, int B, int total,
-                                                    int* __restrict__ plan) {
-  __shared__ int s_blk[1024], s_pad[1024];
+//
+// It also writes the work order of the main kernel (one entry per key block
+// and kv head), longest first ("FlashAttention-4 ...", the paragraph on
+// longest-first scheduling of causal and variable-length work): the
+// (sequence, kv head) pairs sorted by key-block count, most first (ties by
+// sequence index, then kv head), cut into groups of `group` consecutive
+// pairs; the groups in that order, and within a group key block 0 of every
+// pair, then key block 1 of the pairs that have one, and so on.  Under a
+// causal mask key block n of a sequence sees more query rows than block
+// n + 1, so every group starts with its longest units; each pair has a few
+// consecutive key blocks in flight at one time (L2 reuse of its query
+// rows); and block n - 1 of a pair always comes before block n, at most
+// `group` entries earlier (the deterministic mode's ordered additions wait
+// only on earlier units).
+__global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ cu, int B, int total, int Hkv,
+                                                    int group, int* __restrict__ plan, int2* __restrict__ order) {
+  __shared__ int s_blk[1024], s_pad[1024], s_nb[1024], s_seq[1024], s_rnb[1024], s_rpre[1024];
   __shared__ int bad;
   const int t = threadIdx.x;
   if (t == 0) bad = 0;
@@ -221,6 +235,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ cu, 
   }
   s_blk[t] = nb;
   s_pad[t] = np;
+  s_nb[t] = nb;
   __syncthreads();
   // inclusive prefix sums over the 1024 entries
   for (int off = 1; off < 1024; off <<= 1) {
@@ -241,6 +256,48 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* __restrict__ cu, 
     plan[2 * B + 2] = bad ? 0 : s_blk[B - 1];
     plan[2 * B + 3] = bad;
     if (bad && atomicCAS(&g_err.status, 0, FA_ERR_INVALID_ARG) == 0) atomicExch(&g_err.site, 0);
+  }
+  if (bad) return;   // block-uniform: nothing is computed
+
+  // sequences by key-block count, most first (rank r holds sequence s_seq[r])
+  if (t < B) {
+    int rank = 0;
+    for (int c = 0; c < B; ++c) rank += (s_nb[c] > nb) || (s_nb[c] == nb && c < t);
+    s_seq[rank] = t;
+    s_rnb[rank] = nb;
+  }
+  __syncthreads();
+  // exclusive prefix of the ranked counts: pair q = r * Hkv + h starts at
+  // entry Hkv * s_rpre[r] + h * s_rnb[r] of the pair-major enumeration
+  s_rpre[t] = t < B ? s_rnb[t] : 0;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int x = t >= off ? s_rpre[t - off] : 0;
+    __syncthreads();
+    s_rpre[t] += x;
+    __syncthreads();
+  }
+  const int incl = s_rpre[t];
+  __syncthreads();
+  s_rpre[t] = incl - (t < B ? s_rnb[t] : 0);
+  __syncthreads();
+
+  const long long npairs = (long long)B * Hkv;
+  for (long long q = t; q < npairs; q += blockDim.x) {
+    const int r = (int)(q / Hkv), h = (int)(q % Hkv);
+    const int nbq = s_rnb[r];
+    const long long g0 = q - q % group;
+    const long long g1 = g0 + group < npairs ? g0 + group : npairs;
+    // the group's first entry, and its member count at each level n (pairs
+    // with more than n key blocks: a prefix of the group, counts descend)
+    const int r0 = (int)(g0 / Hkv), h0 = (int)(g0 % Hkv);
+    long long pos = (long long)Hkv * s_rpre[r0] + (long long)h0 * s_rnb[r0] + (q - g0);
+    long long members = g1 - g0;
+    for (int n = 0; n < nbq; ++n) {
+      while (members > 0 && s_rnb[(int)((g0 + members - 1) / Hkv)] <= n) --members;
+      order[pos] = make_int2(h * kMaxPackedSeqs + s_seq[r], n);
+      pos += members;
+    }
   }
 }
 
@@ -336,23 +393,15 @@ template <bool PACKED>
 __device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p) {
   Unit w;
   if constexpr (PACKED) {
-    // kv-head-major over the key blocks of all sequences in order: a
-    // sequence's blocks run together, and (deterministic mode) block n - 1
-    // of a sequence always has the smaller unit index
-    const int nb = p.plan[2 * p.B + 2];
-    w.hk = u / nb;
-    const int g = u % nb;
-    int lo = 0, hi = p.B;   // key-block prefix: plan[lo] <= g < plan[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (p.plan[mid] <= g) lo = mid;
-      else hi = mid;
-    }
-    w.b = lo;
-    w.n = g - p.plan[lo];
-    w.qbase = w.kbase = p.cu_seqlens[lo];
-    w.lq = w.lk = p.cu_seqlens[lo + 1] - w.qbase;
-    w.rt = p.plan[p.B + 1 + lo];   // padded-row prefix (multiple of 64)
+    // the order table written by the plan kernel (longest first; block
+    // n - 1 of a pair always has the smaller unit index)
+    const int2 e = p.order[u];
+    w.hk = e.x / kMaxPackedSeqs;
+    w.b = e.x % kMaxPackedSeqs;
+    w.n = e.y;
+    w.qbase = w.kbase = p.cu_seqlens[w.b];
+    w.lq = w.lk = p.cu_seqlens[w.b + 1] - w.qbase;
+    w.rt = p.plan[p.B + 1 + w.b];   // padded-row prefix (multiple of 64)
     w.tk = w.rt / kBM;
   } else {
     // Units in groups of g = sched_group (batch, kv head) pairs; within a
@@ -1000,7 +1049,7 @@ fa_status launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   if (pre_blocks > 16 * L.num_sms) pre_blocks = 16 * L.num_sms;
   if (pre_blocks < 1) pre_blocks = 1;
   if (packed) {
-    bwd::plan_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.Sq, p.plan);
+    bwd::plan_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.Sq, p.Hkv, p.sched_group, p.plan, p.order);
     bwd::pre_packed_kernel<kD><<<(unsigned)pre_blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
         p.cu_seqlens, p.plan, p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq,

@@ -51,8 +51,9 @@ struct BwdParams {
   int* tickets;      // [B, Hq, nqb, 2] (packed: [Hq, nqb, 2]) or nullptr
   const int* cu_seqlens;   // packed layout: device [B + 1]; nullptr for dense
   int* plan;         // packed: key-block prefix [B + 1], padded-row prefix [B + 1], total key blocks, status
+  int2* order;       // packed: work units in schedule order, {kv head * 1024 + sequence, key block}
   int* sched;        // work-unit counter of the dynamic scheduler (zeroed by the pre pass)
-  int sched_group;   // dense: heads per group of the longest-first unit order
+  int sched_group;   // (batch, kv head) / (sequence, kv head) pairs per group of the longest-first unit order
   int sched_dynamic; // 1: units claimed from the counter; 0: CTA c takes units c, c + grid, ...
   int rev_blocks;    // 1: a unit visits its query blocks last to first
   int scores_first;  // 1: the next step's S^T is issued before waiting for the dQ read-out of its buffer
@@ -78,11 +79,11 @@ struct BwdLaunch {
 
 // Workspace carve-up of the backward pass (all offsets 256-byte aligned).
 struct BwdWorkspace {
-  size_t dq_acc, ndelta, nlse2, plan, sched, tickets, total;
+  size_t dq_acc, ndelta, nlse2, plan, order, sched, tickets, total;
   int sq_pad;
 };
 // Dense: rows = Sq per batch entry; packed: Sq = total rows of B sequences.
-BwdWorkspace bwd_workspace_layout(int B, int Hq, int Sq, int D, int deterministic, bool packed);
+BwdWorkspace bwd_workspace_layout(int B, int Hq, int Hkv, int Sq, int D, int deterministic, bool packed);
 
 // 3-D tiled tensor map over a [rows, heads, D] BF16 array (D contiguous) with
 // a box of 64 x 1 x box_rows and 128-byte swizzle.

@@ -101,7 +101,8 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
  *   checked against the layout rules when given.  The size is a bound that
  *   does not depend on the individual lengths: FP32 accumulator [total, Hq, D],
  *   row terms over each sequence's rows rounded up to 64 (Hq x (total rounded
- *   up to 64 + 64 B) each), the per-sequence offset tables and the tickets.
+ *   up to 64 + 64 B) each), the per-sequence offset tables, the order of the
+ *   work units ((total / 128 + B) x Hkv entries of 8 bytes) and the tickets.
  * Returns 0 for arguments fa_bwd() would reject.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, const int* cu_seqlens_host,

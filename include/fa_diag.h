@@ -63,13 +63,15 @@ FA_API fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o,
  *                   work units c, c + grid, ...; 1: each CTA claims its
  *                   next unit from a counter in the workspace (packed
  *                   layouts always claim).
- *   head_group      dense layout: the unit order visits the key blocks of
- *                   head_group (batch, kv head) pairs block by block (block
- *                   0 of each pair, then block 1, ...), group after group;
- *                   1 is head-major, a value >= B * Hkv key-block-major.
- *                   Under a causal mask block 0 is the longest, so this is
- *                   the longest-first order of "FlashAttention-4 ..." (the
- *                   paragraph on longest-first scheduling), per group.
+ *   head_group      the unit order visits the key blocks of head_group
+ *                   (batch, kv head) pairs -- packed layout: (sequence, kv
+ *                   head) pairs, sorted by length, longest first -- block
+ *                   by block (block 0 of each pair, then block 1, ...),
+ *                   group after group; 1 is head-major, a value >= B * Hkv
+ *                   key-block-major.  Under a causal mask block 0 is the
+ *                   longest, so this is the longest-first order of
+ *                   "FlashAttention-4 ..." (the paragraph on longest-first
+ *                   scheduling), per group.
  *   reverse_blocks  1: a unit visits its query blocks last to first.
  *   scores_first    1: the next step's S^T product is issued before the
  *                   MMA warp waits for the dQ read-out of its TMEM buffer;

@@ -102,7 +102,8 @@ def test_packed_workspace_size(lib):
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     B, H, total = 3, 4, 1000
     pad = (total + 63) // 64 * 64 + 64 * B          # row terms per head: every sequence rounded up to 64
-    want = al(total * H * 128 * 4) + 2 * al(H * pad * 4) + al((2 * B + 4) * 4) + 256
+    order = (total // 128 + B) * 2 * 8                # unit order table: (key block, kv head) entries of 8 B
+    want = al(total * H * 128 * 4) + 2 * al(H * pad * 4) + al((2 * B + 4) * 4) + al(order) + 256
     assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total) == want
     assert _ws(lib, B, H, 2, total, total, 128, 1, total_q=total) == want + al(H * (pad // 64) * 2 * 4)
     assert _ws(lib, B, H, 2, total, total, 128, 0, total_q=total, offs=[0, 10, 700, 1000]) == want
