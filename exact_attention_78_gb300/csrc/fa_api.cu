@@ -289,10 +289,12 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.sched = reinterpret_cast<int*>(wb + ws.sched);
     // Work schedule of the main kernel (see its decode_unit and
     // producer_role).  Units are claimed dynamically for packed sequences
-    // (lengths vary without a pattern) and in the deterministic mode;
-    // otherwise CTA c takes units c, c + grid, ..., which measured faster on
-    // dense inputs even under a causal mask (causal S = 1024 / 2048: 567 /
-    // 770 TFLOPS static against 469 / 617 claimed).  Dense order: head-major
+    // (lengths vary without a pattern); otherwise CTA c takes units c,
+    // c + grid, ..., which measured faster on dense inputs even under a
+    // causal mask (causal S = 1024 / 2048: 567 / 770 TFLOPS static against
+    // 469 / 617 claimed; deterministic causal S = 8192 B = 2: 717 against
+    // 696).  In either schedule a unit waits only on units with smaller
+    // indices, which are running or done.  Dense order: head-major
     // (g = 1) without a causal mask (all units equally long; a head's key
     // blocks run together and share its Q / dO rows in L2).  With one,
     // key-block-major within groups of g = 32 heads: the longest blocks start
@@ -313,7 +315,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     // TFLOPS, deterministic 591 / - / 717 / 632 / 569).
     {
       const long long bh = (long long)B * Hkv;
-      const bool dynamic = tune.schedule >= 0 ? tune.schedule == 1 : (packed || deterministic);
+      const bool dynamic = tune.schedule >= 0 ? tune.schedule == 1 : packed;
       long long g = 1;
       if (tune.head_group > 0) g = tune.head_group;
       else if (packed) g = deterministic ? 32 : 16;

@@ -34,9 +34,10 @@
 //
 // Schedules: a static one (CTA c takes units c, c + grid, ...) for dense
 // calls -- head-major without a mask, longest-first (key-block-major) within
-// groups of heads under a causal mask -- and a dynamic one (units claimed from an
-// atomic counter, announced to the roles through a ring in shared memory)
-// for packed and deterministic calls.
+// groups of heads under a causal mask or in deterministic mode -- and a
+// dynamic one (units claimed from an atomic counter, announced to the roles
+// through a ring in shared memory) for packed calls, in the longest-first
+// order the plan kernel writes.
 //
 // Thread layout (512 threads, 16 warps, one CTA per SM; registers per thread
 // after setmaxnreg: elementwise 160, dQ 128, warps 8-11 64):

@@ -109,20 +109,21 @@ __device__ __forceinline__ int num_pairs(const BwdParams& p) { return ((p.Sk + k
 
 __device__ __forceinline__ Unit decode_unit(int u, const BwdParams& p, int rank) {
   Unit w;
+  // Units in groups of g = sched_group (batch, kv head) pairs, pair index m
+  // ascending within a group, each m over the group's heads: g = 1 is
+  // head-major (the clusters working at one time share a head's Q / dO
+  // reads and its dQ-accumulator slice in L2), used without a mask; under a
+  // causal mask pair m sees the most query rows when m is small, so each
+  // group runs longest first; deterministic mode uses g = all heads, which
+  // puts pair m's predecessor (m - 1) of the same head in an earlier wave of
+  // the grid, so the ordered dQ additions rarely wait.
   const int npair = num_pairs(p);
-  int bh;
-  if (p.deterministic) {
-    // pair-major: pair m's predecessor (m - 1) of the same head runs in an
-    // earlier wave of the grid, so the ordered dQ additions rarely wait
-    bh = u % (p.B * p.Hkv);
-    w.m = u / (p.B * p.Hkv);
-  } else {
-    // head-major: the pairs of one (batch, kv head) are adjacent, so the
-    // clusters working at the same time share that head's Q / dO reads and
-    // its slice of the dQ accumulator in L2; causal pairs come longest first
-    bh = u / npair;
-    w.m = u % npair;
-  }
+  const int nbh = p.B * p.Hkv;
+  const int g = p.sched_group;
+  const int grp = u / (g * npair), r = u % (g * npair);
+  const int gh = min(g, nbh - grp * g);   // heads in this (possibly last, smaller) group
+  const int bh = grp * g + r % gh;
+  w.m = r / gh;
   w.b = bh / p.Hkv;
   w.hk = bh % p.Hkv;
   w.n = 2 * w.m + rank;

@@ -57,7 +57,8 @@ FA_API fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o,
  *           distributed shared memory (thousands of cycles of latency that
  *           the fully used tensor memory leaves no room to hide) and runs
  *           at 64 rows per SM.
- * The other knobs apply to the unpaired kernel; negative selects the
+ * The other knobs apply to the unpaired kernel (head_group also orders the
+ * paired kernel's units, pairs of key blocks); negative selects the
  * default, which depends on the call (layout, mask, deterministic mode).
  *   schedule        dense layout: 0: CTA c of the persistent grid takes
  *                   work units c, c + grid, ...; 1: each CTA claims its

@@ -140,3 +140,24 @@ def test_packed_orders_match_oracle(fa, deterministic, tuning):
                 continue
             e = rel_fro(got, ref)
             assert e <= GRAD_RTOL, (s_, name, e)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("group", [1, 3, 64])
+def test_paired_kernel_head_groups(fa, causal, deterministic, group):
+    """The paired-CTA kernel under every head grouping of its unit order
+    (pairs of key blocks, longest first within a group)."""
+    q, k, v, do = _inputs(2, 4, 2, 700, 700, seed=25)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal=causal)
+    runs = []
+    for _ in range(2 if deterministic else 1):
+        g = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, deterministic=deterministic, paired=True,
+                   tuning={"head_group": group})
+        assert fa.get_device_error() == 0
+        runs.append(tuple(t.cpu() for t in g))
+    if deterministic:
+        for x, y in zip(*runs):
+            assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    _check_dense(runs[0], q, k, v, do, causal)
