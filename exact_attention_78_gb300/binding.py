@@ -101,6 +101,20 @@ def _check_bf16(name, t):
         raise ValueError("%s must be a contiguous CUDA bfloat16 tensor" % name)
 
 
+def _check_out(name, t, shape, dtype, device):
+    """A caller-supplied output buffer: the library writes shape x dtype
+    elements at its address, so anything else is refused here."""
+    if (not t.is_cuda or t.device != device or t.dtype != dtype or not t.is_contiguous()
+            or tuple(t.shape) != tuple(shape)):
+        raise ValueError("%s must be a contiguous %s tensor of shape %s on %s" % (name, dtype, tuple(shape), device))
+
+
+def _check_same_device(device, **tensors):
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError("%s is on %s, q on %s" % (name, t.device, device))
+
+
 def _dims(q, k, cu_seqlens):
     """(B, Hq, Hkv, Sq, Sk, D) as the C ABI wants them."""
     if cu_seqlens is None:
@@ -111,8 +125,8 @@ def _dims(q, k, cu_seqlens):
     else:
         if q.dim() != 3 or k.dim() != 3:
             raise ValueError("packed q/k/v are [total, H, D]")
-        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
-            raise ValueError("cu_seqlens must be a CUDA int32 tensor")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or not cu_seqlens.is_contiguous():
+            raise ValueError("cu_seqlens must be a contiguous CUDA int32 tensor")
         B = cu_seqlens.numel() - 1
         Sq, Hq, D = q.shape
         Sk, Hkv = k.shape[0], k.shape[1]
@@ -125,25 +139,31 @@ def fwd(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, 
     lib = load_library()
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n, t)
+    _check_same_device(q.device, k=k, v=v, cu_seqlens=cu_seqlens)
     B, Hq, Hkv, Sq, Sk, D = _dims(q, k, cu_seqlens)
     if scale is None:
         scale = D ** -0.5
+    lse_shape = (Hq, Sq) if cu_seqlens is not None else (B, Hq, Sq)
     if out is None:
         out = torch.empty_like(q)
+    else:
+        _check_out("out", out, q.shape, torch.bfloat16, q.device)
     if lse is None:
-        shape = (Hq, Sq) if cu_seqlens is not None else (B, Hq, Sq)
-        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    else:
+        _check_out("lse", lse, lse_shape, torch.float32, q.device)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
             float(scale), _ptr(cu_seqlens)]
-    if rescale_threshold is None and emu_per_16 is None:
-        st = lib.fa_fwd(*args, _stream(stream))
-    else:
-        t = lib.fa_fwd_default_tuning()
-        if rescale_threshold is not None:
-            t.rescale_threshold = float(rescale_threshold)
-        if emu_per_16 is not None:
-            t.emu_per_16 = int(emu_per_16)
-        st = lib.fa_fwd_ex(*args, ctypes.byref(t), _stream(stream))
+    with torch.cuda.device(q.device):   # the library launches on the current device
+        if rescale_threshold is None and emu_per_16 is None:
+            st = lib.fa_fwd(*args, _stream(stream))
+        else:
+            t = lib.fa_fwd_default_tuning()
+            if rescale_threshold is not None:
+                t.rescale_threshold = float(rescale_threshold)
+            if emu_per_16 is not None:
+                t.emu_per_16 = int(emu_per_16)
+            st = lib.fa_fwd_ex(*args, ctypes.byref(t), _stream(stream))
     _check(st, "fa_fwd")
     return out, lse
 
@@ -172,27 +192,41 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, work
     lib = load_library()
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
         _check_bf16(n, t)
+    _check_same_device(q.device, k=k, v=v, o=o, lse=lse, do=do, cu_seqlens=cu_seqlens)
     B, Hq, Hkv, Sq, Sk, D = _dims(q, k, cu_seqlens)
+    if tuple(o.shape) != tuple(q.shape) or tuple(do.shape) != tuple(q.shape):
+        raise ValueError("o and do must have q's shape %s" % (tuple(q.shape),))
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError("v must have k's shape %s" % (tuple(k.shape),))
+    lse_shape = (Hq, Sq) if cu_seqlens is not None else (B, Hq, Sq)
+    if not lse.is_cuda or lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != lse_shape:
+        raise ValueError("lse must be a contiguous CUDA float32 tensor of shape %s" % (lse_shape,))
     if scale is None:
         scale = D ** -0.5
     need = bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, deterministic, total_q=Sq if cu_seqlens is not None else 0)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    elif not workspace.is_cuda or workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on %s" % q.device)
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t is not None:
+            _check_out(name, t, like.shape, torch.bfloat16, q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq,
             Sk, D, int(bool(causal)), float(scale), _ptr(cu_seqlens), int(bool(deterministic)), _ptr(workspace),
-            workspace.numel()]
-    if paired is None and not tuning:
-        st = lib.fa_bwd(*args, _stream(stream))
-    else:
-        t = lib.fa_bwd_default_tuning()
-        if paired is not None:
-            t.paired = int(bool(paired))
-        for name, val in (tuning or {}).items():
-            setattr(t, name, int(val))
-        st = lib.fa_bwd_ex(*args, ctypes.byref(t), _stream(stream))
+            workspace.numel() * workspace.element_size()]
+    with torch.cuda.device(q.device):   # the library launches on the current device
+        if paired is None and not tuning:
+            st = lib.fa_bwd(*args, _stream(stream))
+        else:
+            t = lib.fa_bwd_default_tuning()
+            if paired is not None:
+                t.paired = int(bool(paired))
+            for name, val in (tuning or {}).items():
+                setattr(t, name, int(val))
+            st = lib.fa_bwd_ex(*args, ctypes.byref(t), _stream(stream))
     _check(st, "fa_bwd")
     return dq, dk, dv
 

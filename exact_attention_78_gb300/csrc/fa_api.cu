@@ -8,6 +8,8 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "fa.h"
 #include "fa_diag.h"
@@ -78,6 +80,20 @@ fa_status check_shapes(int B, int Hq, int Hkv, int Sq, int Sk, int D, float scal
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
+
+fa_status prepare_kernel(const void* func, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;   // (kernel, device)
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : done)
+    if (e.first == func && e.second == dev) return FA_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return FA_ERR_CUDA;
+  done.emplace_back(func, dev);
+  return FA_OK;
+}
 
 fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_rows) {
   auto fn = encode_fn();

@@ -1072,17 +1072,13 @@ fa_status launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
     if ((st = make_tmap_rows_heads_d(&tdo, p.dout, rows_q, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
     if ((st = make_tmap_rows_heads_d(&tk, L.k, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
     if ((st = make_tmap_rows_heads_d(&tv, L.v, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
-    static bool attr_done = false;
-    if (!attr_done) {
-      if (cudaFuncSetAttribute(bwd::bwd_kernel<kD, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               bwd::Layout<kD>::kDynamic) != cudaSuccess ||
-          cudaFuncSetAttribute(bwd::bwd_kernel<kD, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               bwd::Layout<kD>::kDynamic) != cudaSuccess ||
-          cudaFuncSetAttribute(bwd::bwd_kernel<kD, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               bwd::Layout<kD>::kDynamic) != cudaSuccess)
-        return FA_ERR_CUDA;
-      attr_done = true;
-    }
+    if ((st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, false, false>),
+                             bwd::Layout<kD>::kDynamic)) != FA_OK ||
+        (st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, false, true>),
+                             bwd::Layout<kD>::kDynamic)) != FA_OK ||
+        (st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, true, true>),
+                             bwd::Layout<kD>::kDynamic)) != FA_OK)
+      return st;
     // packed: the number of key blocks is only known on the device; this
     // bound (every sequence adds at most one partial block) sizes the grid
     const long long units = packed ? ((long long)p.Sk / bwd::kBN + p.B) * p.Hkv

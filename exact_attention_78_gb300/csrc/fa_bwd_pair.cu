@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -717,16 +718,26 @@ fa_status launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
-    if (cudaFuncSetAttribute(bwdp::bwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bwdp::Layout::kDynamic) != cudaSuccess)
-      return FA_ERR_CUDA;
-    cfg.gridDim = dim3(2 * (L.num_sms / 2), 1, 1);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bwdp::bwd_pair_kernel, &cfg) != cudaSuccess || n < 1)
-      return FA_ERR_CUDA;
-    max_clusters = n;
+  if ((st = prepare_kernel(reinterpret_cast<const void*>(bwdp::bwd_pair_kernel), bwdp::Layout::kDynamic)) != FA_OK)
+    return st;
+  // resident clusters per device, computed once per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  constexpr int kMaxDevices = 64;
+  static int resident[kMaxDevices] = {};
+  static std::mutex mu;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    if (resident[dev] == 0) {
+      cfg.gridDim = dim3(2 * (L.num_sms / 2), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, bwdp::bwd_pair_kernel, &cfg) != cudaSuccess || n < 1)
+        return FA_ERR_CUDA;
+      resident[dev] = n;
+    }
+    max_clusters = resident[dev];
   }
   // as many clusters as can be resident at once: the deterministic mode's
   // ordered additions then only ever wait on running clusters

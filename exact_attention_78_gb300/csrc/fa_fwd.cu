@@ -699,12 +699,8 @@ fa_status launch_inst(const FwdLaunch& L, const CUtensorMap& tq, const CUtensorM
                       cudaStream_t stream) {
   using Lay = Layout<D, VARLEN>;
   auto kern = fwd_kernel<D, CAUSAL, VARLEN, EMU>;
-  static bool attr_done = false;  // per instantiation
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kDynamic) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_done = true;
-  }
+  const fa_status st = prepare_kernel(reinterpret_cast<const void*>(kern), Lay::kDynamic);
+  if (st != FA_OK) return st;
   int grid = L.num_sms;
   if (!VARLEN) {
     const long long units = (long long)((L.p.Sq + kPairRows - 1) / kPairRows) * L.p.B * L.p.Hq;

@@ -93,6 +93,11 @@ fa_status make_tmap_rows_heads_d(CUtensorMap* map, const void* base, int rows, i
 fa_status make_tmap_f32_rows_heads_d(CUtensorMap* map, const void* base, int rows, int heads, int D, int box_d,
                                      int box_rows);
 
+// Raises the dynamic shared-memory limit of kernel `func` to `bytes` the
+// first time it is launched on the current device (the attribute is per
+// device); thread-safe.
+fa_status prepare_kernel(const void* func, int bytes);
+
 // Kernel launchers (defined in their translation units).
 fa_status launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream);
