@@ -255,7 +255,13 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     if ws > 1:
         replicas.init("nccl", device=torch.device("cuda", local))
-    fa.load_library(build_if_missing=(rank == 0))
+    # rank 0 builds the library if it is missing or stale; the others load
+    # it once rank 0 is done
+    if rank == 0:
+        fa.load_library(build_if_missing=True)
+    if ws > 1:
+        replicas.barrier()
+    fa.load_library()
     w = workload(args)
     (q, k, v, do), cu = W.make_inputs(w, with_grad=True)
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
@@ -271,21 +277,18 @@ def run_gpu(args):
     have_bwd = not args.fwd_only
     ws_buf = dq = dk = dv = None
     if have_bwd:
-        try:
-            if w.packed:
-                rows = qd.shape[0]
-                need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, rows, rows, w.D, det, total_q=rows)
-            else:
-                need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, det)
-            ws_buf = torch.empty(need, dtype=torch.uint8, device="cuda")
-            dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-            fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, emu_per_16=args.emu)
-            fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
-                   dv=dv, paired=paired, cu_seqlens=cud, tuning=tuning)
-        except fa.FAError as e:
-            if e.status != 2:
-                raise
-            have_bwd = False
+        # an unsupported backward configuration raises here: the step is
+        # never silently reduced to the forward
+        if w.packed:
+            rows = qd.shape[0]
+            need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, rows, rows, w.D, det, total_q=rows)
+        else:
+            need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, det)
+        ws_buf = torch.empty(need, dtype=torch.uint8, device="cuda")
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, emu_per_16=args.emu)
+        fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
+               dv=dv, paired=paired, cu_seqlens=cud, tuning=tuning)
     torch.cuda.synchronize()
 
     ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -419,6 +422,8 @@ def run_gpu(args):
     peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": measured_traffic(kname, w), "kernel": kname,
+                "timed": ("the whole backward call (its pre, main and post kernels), CUDA events on its stream"
+                          if dom == "bwd" else "the forward call (one kernel), CUDA events on its stream"),
                 "peak_kind": "%s, sustained bf16 (kernel timed inside a repeated step)" % pk_kind}
 
     cpu = None
@@ -441,7 +446,9 @@ def run_gpu(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (1 + (3 if have_bwd else 0)),
+        # per step: the forward kernel; the backward's pre, main and post
+        # kernels (packed layout: plus the offset-checking plan kernel)
+        "gpu_launches": args.steps * (1 + ((4 if w.packed else 3) if have_bwd else 0)),
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
