@@ -166,3 +166,26 @@ def test_python_binding_fails_loudly_without_cuda_tensors():
     x = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fwd(x, x, x)
+
+
+def test_headers_compile_as_c99_and_link(lib, tmp_path):
+    """The public headers are plain C: a C99 program (strict, warnings as
+    errors) includes both, links the shared library, and its struct sizes
+    match the Python binding's."""
+    import shutil
+    import subprocess
+    from exact_attention_78_gb300 import binding
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    so = binding.lib_path()
+    exe = str(tmp_path / "abi_consumer")
+    subprocess.run([gcc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "abi_consumer.c"), "-o", exe, "-L", os.path.dirname(so),
+                    "-l:" + os.path.basename(so), "-Wl,-rpath," + os.path.dirname(so)],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=60).stdout
+    sizes = dict(line.rsplit(" ", 1) for line in out.splitlines() if line.startswith("sizeof"))
+    assert int(sizes["sizeof fa_fwd_tuning"]) == ctypes.sizeof(binding.FwdTuning)
+    assert int(sizes["sizeof fa_bwd_tuning"]) == ctypes.sizeof(binding.BwdTuning)
+    assert "status FA_ERR_WORKSPACE" in out
