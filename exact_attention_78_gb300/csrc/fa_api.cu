@@ -293,6 +293,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.dq = dq;
     L.p.dk = dk;
     L.p.dv = dv;
+    L.p.dkv_st32 = ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 31u) == 0;
     L.p.dq_acc = reinterpret_cast<float*>(wb + ws.dq_acc);
     L.p.ndelta = reinterpret_cast<float*>(wb + ws.ndelta);
     L.p.nlse2 = reinterpret_cast<float*>(wb + ws.nlse2);

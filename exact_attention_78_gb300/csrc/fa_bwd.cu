@@ -833,14 +833,20 @@ __device__ void dq_role(const Shared<kD>& sh, const uint32_t tmem, const BwdPara
           for (int e = 0; e < 32; ++e) r[e] = 0u;
         }
         if (valid) {
+          // 32 columns of this key row: 64 contiguous bytes, as two 32-byte
+          // stores (whole L2 sectors) when dK and dV allow it, else four
+          // 16-byte ones
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * mul, __uint_as_float(r[8 * e + 1]) * mul);
-            o.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * mul, __uint_as_float(r[8 * e + 3]) * mul);
-            o.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * mul, __uint_as_float(r[8 * e + 5]) * mul);
-            o.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * mul, __uint_as_float(r[8 * e + 7]) * mul);
-            reinterpret_cast<uint4*>(dst + c * 32)[e] = o;
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+          if (p.dkv_st32) {
+            st_global_v8(dst + c * 32, pk);
+            st_global_v8(dst + c * 32 + 16, pk + 8);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              reinterpret_cast<uint4*>(dst + c * 32)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
           }
         }
       }

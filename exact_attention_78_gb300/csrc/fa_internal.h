@@ -56,6 +56,7 @@ struct BwdParams {
   int sched_group;   // (batch, kv head) / (sequence, kv head) pairs per group of the longest-first unit order
   int sched_dynamic; // 1: units claimed from the counter; 0: CTA c takes units c, c + grid, ...
   int rev_blocks;    // 1: a unit visits its query blocks last to first
+  int dkv_st32;      // dK and dV are 32-byte aligned: their rows are written with 32-byte stores
   int scores_first;  // 1: the next step's S^T is issued before waiting for the dQ read-out of its buffer
   int B, Hq, Hkv, Sq, Sk, D;   // packed: Sq = Sk = total rows
   int sq_pad;        // row-term floats per head: dense Sq rounded up to 64, packed Sq rounded up + 64 B

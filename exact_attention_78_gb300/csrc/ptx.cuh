@@ -231,6 +231,14 @@ FA_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.rea
 FA_DEV void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Wait until all committed bulk groups have completed (writes performed).
 FA_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// 32-byte store of eight words (the address must be 32-byte aligned): one
+// full L2 sector per thread.
+FA_DEV void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Orders this thread's global-memory accesses made through the async proxy
 // (TMA, bulk copies and reductions) with its generic-proxy accesses.
 FA_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
