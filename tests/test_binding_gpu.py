@@ -62,3 +62,25 @@ def test_workspace_is_sized_in_bytes(fa):
     with pytest.raises(fa.FAError) as e:
         fa.bwd(q, k, v, o, lse, do, workspace=torch.empty(need // 4 - 1, dtype=torch.float32, device="cuda"))
     assert e.value.status == 5
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_gradients_into_16_byte_aligned_buffers(fa, D):
+    """dK and dV rows are written with 32-byte stores when both buffers are
+    32-byte aligned and with 16-byte stores otherwise (the ABI asks for 16).
+    In deterministic mode the two paths must give the same bits."""
+    q, k, v, do = _qkv(B=1, H=2, S=300, D=D)
+    o, lse = fa.fwd(q, k, v, causal=True)
+    ref = fa.bwd(q, k, v, o, lse, do, causal=True, deterministic=True)
+
+    def offset_like(t):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+        view = buf[8:].view(t.shape)            # 16 bytes past a 512-byte-aligned allocation
+        assert view.data_ptr() % 32 == 16
+        return view
+
+    dq, dk, dv = offset_like(q), offset_like(k), offset_like(v)
+    got = fa.bwd(q, k, v, o, lse, do, causal=True, deterministic=True, dq=dq, dk=dk, dv=dv)
+    assert fa.get_device_error() == 0
+    for a, b in zip(ref, got):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
