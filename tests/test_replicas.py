@@ -30,7 +30,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_two_gloo_ranks():
     world, port = 2, _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()   # no fork of this multi-threaded process
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1] == 12.5
 
