@@ -24,7 +24,8 @@ class FAError(RuntimeError):
 
 
 class FwdTuning(ctypes.Structure):
-    _fields_ = [("rescale_threshold", ctypes.c_float), ("emu_per_16", ctypes.c_int)]
+    _fields_ = [("rescale_threshold", ctypes.c_float), ("emu_per_16", ctypes.c_int), ("split_p", ctypes.c_int),
+                ("kv_stages", ctypes.c_int), ("head_group", ctypes.c_int)]
 
 
 class BwdTuning(ctypes.Structure):
@@ -134,8 +135,10 @@ def _dims(q, k, cu_seqlens):
 
 
 def fwd(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, rescale_threshold=None,
-        emu_per_16=None, stream=None):
-    """O, LSE = attention(q, k, v).  Dense [B,S,H,D] or packed [total,H,D]."""
+        emu_per_16=None, split_p=None, kv_stages=None, head_group=None, stream=None):
+    """O, LSE = attention(q, k, v).  Dense [B,S,H,D] or packed [total,H,D].
+    rescale_threshold, emu_per_16, split_p, kv_stages and head_group override
+    the library's per-configuration choices (fa_fwd_tuning)."""
     lib = load_library()
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n, t)
@@ -155,14 +158,16 @@ def fwd(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, 
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, int(bool(causal)),
             float(scale), _ptr(cu_seqlens)]
     with torch.cuda.device(q.device):   # the library launches on the current device
-        if rescale_threshold is None and emu_per_16 is None:
+        knobs = {"emu_per_16": emu_per_16, "split_p": split_p, "kv_stages": kv_stages, "head_group": head_group}
+        if rescale_threshold is None and all(x is None for x in knobs.values()):
             st = lib.fa_fwd(*args, _stream(stream))
         else:
             t = lib.fa_fwd_default_tuning()
             if rescale_threshold is not None:
                 t.rescale_threshold = float(rescale_threshold)
-            if emu_per_16 is not None:
-                t.emu_per_16 = int(emu_per_16)
+            for name, val in knobs.items():
+                if val is not None:
+                    setattr(t, name, int(val))
             st = lib.fa_fwd_ex(*args, ctypes.byref(t), _stream(stream))
     _check(st, "fa_fwd")
     return out, lse

@@ -18,15 +18,37 @@
 namespace fa {
 namespace {
 
-// -1: chosen per configuration by default_emu_per_16().
-constexpr int kDefaultEmuPer16 = -1;
+// Forward knobs the library picks per configuration when the caller leaves
+// them at -1.
+struct FwdChoice {
+  int emu_per_16;   // exponentials of every 16 on the FMA-pipe polynomial
+  int split_p;      // P handed to the tensor cores in two halves
+  int kv_stages;    // K/V ring depth
+  int head_group;   // dense causal: (batch, head) pairs per longest-first group
+};
 
-// Share of the softmax exponentials computed by the FMA-pipe polynomial
-// (of every 16) when the caller leaves it to the library: measured on GB300
-// (B=8, S=4096, forward TFLOPS for 0 / 2 / 3 / 4 of 16): D=128 causal
-// 1126 / 1158 / 1116 / 1116; D=128 non-causal 1403 / 1369 / 1355 / 1356;
-// D=64 non-causal 814 / 810 / 677 / 677 and causal 668 / 665 / 606 / 607.
-int default_emu_per_16(int D, int causal) { return (D == 128 && causal) ? 2 : 0; }
+// The table of per-configuration choices, from a measured sweep on GB300
+// (forward TFLOPS, B*S = 32768 tokens, H = 16, S = 1K ... 32K; the full
+// sweep is in the design notes).  Handing P over in two halves (split_p)
+// paid everywhere, and with it moving 2 of every 16 exponentials to the FMA
+// pipe did too (D = 128, S = 4096: 1294 with neither, 1336 split, 1405 split
+// with 2/16; causal 1058 / 1058 / 1128; D = 64 non-causal 709 / 714 / 772);
+// 4/16 on the FMA pipe was slower than 2/16 everywhere.  The K/V ring: D = 128
+// keeps its maximum of 4 stages (2: -5 to -10%; 3: equal or within noise);
+// D = 64 is flat from 4 to 8 stages and loses a little at 10 under a causal
+// mask; it takes 6.
+FwdChoice default_fwd_choice(int D, int causal, int Sk, int BH) {
+  FwdChoice c;
+  c.emu_per_16 = 2;
+  c.split_p = 1;
+  c.kv_stages = D == 128 ? 4 : 6;
+  // all heads in one longest-first group: groups of 8 / 32 heads measured
+  // 1-4% slower at S = 1024 and 4096 (causal D = 128)
+  c.head_group = BH;
+  (void)causal;
+  (void)Sk;
+  return c;
+}
 constexpr float kDefaultThreshold = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -160,7 +182,10 @@ extern "C" {
 fa_fwd_tuning fa_fwd_default_tuning(void) {
   fa_fwd_tuning t;
   t.rescale_threshold = kDefaultThreshold;
-  t.emu_per_16 = kDefaultEmuPer16;
+  t.emu_per_16 = -1;
+  t.split_p = -1;
+  t.kv_stages = -1;
+  t.head_group = -1;
   return t;
 }
 
@@ -183,7 +208,15 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
           return FA_ERR_INVALID_ARG;
         tune.emu_per_16 = t->emu_per_16;
       }
+      if (t->split_p > 1) return FA_ERR_INVALID_ARG;
+      tune.split_p = t->split_p;
+      if (t->kv_stages > 0) {
+        if (t->kv_stages < 2 || t->kv_stages > (D == 128 ? 4 : 10)) return FA_ERR_INVALID_ARG;
+        tune.kv_stages = t->kv_stages;
+      }
+      tune.head_group = t->head_group;
     }
+    const FwdChoice def = default_fwd_choice(D, causal, Sk, B * Hq);
     int num_sms = 0;
     if ((st = device_info(&num_sms)) != FA_OK) return st;
     FwdLaunch L{};
@@ -201,10 +234,19 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
     L.p.group = Hq / Hkv;
     L.p.scale_log2 = scale * kLog2e;
     L.p.thr = tune.rescale_threshold;
+    L.p.stages = tune.kv_stages > 0 ? tune.kv_stages : def.kv_stages;
+    L.p.split_p = tune.split_p >= 0 ? tune.split_p : def.split_p;
+    {
+      const long long bh = (long long)B * Hq;
+      long long g = tune.head_group > 0 ? tune.head_group : def.head_group;
+      if (g > bh) g = bh;
+      if (g < 1) g = 1;
+      L.p.sched_group = (int)g;
+    }
     L.p.wait_limit_ns = kDefaultWaitLimitNs;
     L.D = D;
     L.causal = causal != 0;
-    L.emu_per_16 = tune.emu_per_16 >= 0 ? tune.emu_per_16 : default_emu_per_16(D, causal);
+    L.emu_per_16 = tune.emu_per_16 >= 0 ? tune.emu_per_16 : def.emu_per_16;
     L.num_sms = num_sms;
     return launch_fwd(L, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {

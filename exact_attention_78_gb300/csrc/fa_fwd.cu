@@ -69,12 +69,12 @@ struct Layout {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kBM * D * 2;     // 128 rows x D BF16
   static constexpr int kChunkBytes = kBM * 128;      // 128 rows x 64 BF16
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  // K/V ring depth: chosen per call (FwdParams::stages), at most this many
+  static constexpr int kMaxStages = (D == 128) ? 4 : 10;
   static constexpr int kQ = 0;
-  static constexpr int kKV = kQ + 2 * kTileBytes;
-  static constexpr int kBars = kKV + kStages * kTileBytes;
-  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_ready[2], o_ready[2], o_full[2]
-  static constexpr int kNumBars = 2 + 2 * kStages + 8;
+  static constexpr int kBars = kQ + 2 * kTileBytes;
+  // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_lo[2], p_hi[2], o_ready[2], o_full[2]
+  static constexpr int kNumBars = 2 + 2 * kMaxStages + 10;
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem slot, abort, warp flags[8]
   static constexpr int kStats = kMisc + 64;            // scale/l/m/lr: 4 x [2][128] floats
   static constexpr int kSched = kStats + 4 * 2 * kBM * 4;
@@ -82,9 +82,11 @@ struct Layout {
   // pair-group prefix [P+1], header[4]  (ints)
   static constexpr int kSchedInts = 3 * kMaxPackedSeqs + (kMaxPackedSeqs + 1) + (kMaxPairsPerSeq + 1) + 4;
   static constexpr int kSchedBytes = VARLEN ? 4 * kSchedInts : 0;
-  static constexpr int kTotal = kSched + kSchedBytes;
-  static constexpr int kDynamic = kTotal + kSmemAlignSlack;
-  static_assert(kDynamic <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+  // the K/V ring last, 1024-byte aligned (whole 128-byte swizzle atoms)
+  static constexpr int kKV = (kSched + kSchedBytes + 1023) / 1024 * 1024;
+  static constexpr int dynamic_bytes(int stages) { return kKV + stages * kTileBytes + kSmemAlignSlack; }
+  static constexpr int kMaxDynamic = kKV + kMaxStages * kTileBytes + kSmemAlignSlack;
+  static_assert(kMaxDynamic <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
 // One work unit: a pair of 128-row query tiles of one (sequence, head).
@@ -95,7 +97,8 @@ struct Unit {
   int k_tok0;     // same for keys
   int seq_q, seq_k;
   int b;          // batch / sequence index (for LSE addressing)
-  int n;          // KV blocks to visit
+  int nt[2];      // KV blocks each query tile sees (0: no valid row, or no visible key)
+  int n;          // KV blocks to load: max(nt[0], nt[1])
 };
 
 // Packed-length schedule tables (shared memory).  Sequences are sorted by
@@ -109,12 +112,17 @@ struct PackedSched {
   int* header;     // [0] total units, [1] max pairs P, [2] total tokens, [3] bad input
 };
 
+// KV blocks the query tile starting at row `row0` needs: 0 when the tile has
+// no valid row; under the causal mask up to the block holding the last key
+// its last valid row sees (row r sees keys <= r + (seq_k - seq_q)).  Tile 0 of
+// a causal pair skips the block that only tile 1 sees.
 template <bool CAUSAL>
-__device__ __forceinline__ int unit_kv_blocks(int pair, int seq_q, int seq_k) {
+__device__ __forceinline__ int tile_kv_blocks(int row0, int seq_q, int seq_k) {
+  if (row0 >= seq_q) return 0;
   int kv_end = seq_k;
   if (CAUSAL) {
-    // the pair's last row (pair*256 + 255) sees keys <= row + (seq_k - seq_q)
-    kv_end = min(seq_k, pair * kPairRows + kPairRows + (seq_k - seq_q));
+    const int last = min(row0 + kBM, seq_q) - 1;
+    kv_end = min(seq_k, last + 1 + (seq_k - seq_q));
   }
   return kv_end <= 0 ? 0 : (kv_end + kBN - 1) / kBN;
 }
@@ -126,9 +134,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p, const Pac
     const int npairs = (p.Sq + kPairRows - 1) / kPairRows;
     const int BH = p.B * p.Hq;
     int bh;
-    if (CAUSAL) {  // longest first: pairs near the end of the sequence first
-      w.pair = npairs - 1 - u / BH;
-      bh = u % BH;
+    if (CAUSAL) {
+      // longest first within groups of sched_group (batch, head) pairs: a
+      // group's pairs near the end of the sequence (the most key blocks)
+      // first, every head of the group at each level, group after group.
+      // The groups bound how many heads' K/V are in flight at once, so that
+      // the key blocks a head's pairs share stay in L2.
+      const int G = p.sched_group;
+      const int grp = u / (G * npairs), r = u % (G * npairs);
+      const int gh = min(G, BH - grp * G);   // heads of this (possibly last, smaller) group
+      w.pair = npairs - 1 - r / gh;
+      bh = grp * G + r % gh;
     } else {       // every pair costs the same: keep a head's pairs together
       bh = u / npairs;
       w.pair = u % npairs;
@@ -173,7 +189,9 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p, const Pac
     w.seq_q = ps.len[i];
     w.seq_k = ps.len[i];
   }
-  w.n = unit_kv_blocks<CAUSAL>(w.pair, w.seq_q, w.seq_k);
+  w.nt[0] = tile_kv_blocks<CAUSAL>(w.pair * kPairRows, w.seq_q, w.seq_k);
+  w.nt[1] = tile_kv_blocks<CAUSAL>(w.pair * kPairRows + kBM, w.seq_q, w.seq_k);
+  w.n = max(w.nt[0], w.nt[1]);
   return w;
 }
 
@@ -243,6 +261,16 @@ __device__ int build_packed_sched(const FwdParams& p, PackedSched& ps, uint8_t* 
   return ps.header[0];
 }
 
+// Position in the K/V ring: stage index and the parity of its barriers'
+// current phase, advanced without a division by the (run-time) ring depth.
+struct RingPos {
+  int stage;
+  uint32_t phase;
+};
+FA_DEV RingPos ring_next(RingPos r, int stages) {
+  return (r.stage + 1 == stages) ? RingPos{0, r.phase ^ 1u} : RingPos{r.stage + 1, r.phase};
+}
+
 // Shared-memory handles.  Barriers and the abort flag are addressed through
 // 32-bit shared-window addresses to keep the issue warps' register use low.
 template <int D, bool VARLEN>
@@ -254,11 +282,14 @@ struct Shared {
   FA_DEV uint32_t q_full() const { return bar(0); }
   FA_DEV uint32_t q_empty() const { return bar(1); }
   FA_DEV uint32_t kv_full(int s) const { return bar(2 + s); }
-  FA_DEV uint32_t kv_empty(int s) const { return bar(2 + L::kStages + s); }
-  FA_DEV uint32_t s_full(int t) const { return bar(2 + 2 * L::kStages + t); }
-  FA_DEV uint32_t p_ready(int t) const { return bar(4 + 2 * L::kStages + t); }
-  FA_DEV uint32_t o_ready(int t) const { return bar(6 + 2 * L::kStages + t); }
-  FA_DEV uint32_t o_full(int t) const { return bar(8 + 2 * L::kStages + t); }
+  FA_DEV uint32_t kv_empty(int s) const { return bar(2 + L::kMaxStages + s); }
+  FA_DEV uint32_t s_full(int t) const { return bar(2 + 2 * L::kMaxStages + t); }
+  // P of tile t written: keys 0-63 (p_lo) and keys 64-127 (p_hi); one
+  // arrival per softmax thread
+  FA_DEV uint32_t p_lo(int t) const { return bar(4 + 2 * L::kMaxStages + t); }
+  FA_DEV uint32_t p_hi(int t) const { return bar(6 + 2 * L::kMaxStages + t); }
+  FA_DEV uint32_t o_ready(int t) const { return bar(8 + 2 * L::kMaxStages + t); }
+  FA_DEV uint32_t o_full(int t) const { return bar(10 + 2 * L::kMaxStages + t); }
   FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
   FA_DEV uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + L::kMisc); }
   FA_DEV int* warp_flag() const { return reinterpret_cast<int*>(base + L::kMisc + 8); }   // [2][4]
@@ -282,12 +313,13 @@ __device__ void softmax_role(const int t, const Shared<D, VARLEN>& sh, const uin
   uint32_t sit = 0;
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
-    if (w.n == 0) continue;
+    const int nt = t ? w.nt[1] : w.nt[0];   // (no dynamic index into the struct's array)
+    if (nt == 0) continue;
     const int tile_row0 = w.pair * kPairRows + t * kBM;
     const int row = tile_row0 + r_in_tile;
     const int diag = w.seq_k - w.seq_q;
     float m_run = -INFINITY, l_run = 0.0f, lr_run = 0.0f;
-    for (int j = 0; j < w.n; ++j, ++sit) {
+    for (int j = 0; j < nt; ++j, ++sit) {
       if (!mbar_wait_bounded(sh.s_full(t), sit & 1, sh.abort(), &g_err, kSiteSoftmaxS, p.wait_limit_ns)) return;
       tc_fence_after();
       uint32_t r[4][32];
@@ -335,37 +367,57 @@ __device__ void softmax_role(const int t, const Shared<D, VARLEN>& sh, const uin
       // go through packed FP32x2 instructions.
       const uint64_t sl2x2 = pk2(sl2, sl2), negm2 = pk2(-m_use, -m_use);
       uint64_t se2[4] = {0ull, 0ull, 0ull, 0ull}, sr2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[2][32];
+      // P in two halves of 64 keys, each as BF16 pairs over 32 TMEM columns
+      // (the first 64 columns of S).  With split_p the first half is
+      // signalled on its own, so the PV product over keys 0-63 may start
+      // while the exponentials of keys 64-127 are still being computed
+      // ("FlashAttention-4: matrix throughput bottlenecks", section "Keep
+      // tiles moving without overwriting live data": an initial portion of
+      // the coefficients is announced before the rest, which is protected by
+      // its own synchronisation).
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const uint64_t x2 = fma2(pk2(__uint_as_float(r[c / 32][c % 32]), __uint_as_float(r[c / 32][c % 32 + 1])),
-                                 sl2x2, negm2);
-        float x0, x1, e0, e1;
-        up2(x2, x0, x1);
-        exp2_pair<EMU>(x0, x1, c, e0, e1);
-        const uint32_t pp = pack_bf16x2(e0, e1);
-        pk[c / 64][(c / 2) % 32] = pp;
-        se2[(c / 2) & 3] = add2(se2[(c / 2) & 3], pk2(e0, e1));
-        sr2[(c / 2) & 3] = add2(sr2[(c / 2) & 3], pk2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u)));
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 64 * half; c < 64 * half + 64; c += 2) {
+          const uint64_t x2 = fma2(pk2(__uint_as_float(r[c / 32][c % 32]), __uint_as_float(r[c / 32][c % 32 + 1])),
+                                   sl2x2, negm2);
+          float x0, x1, e0, e1;
+          up2(x2, x0, x1);
+          exp2_pair<EMU>(x0, x1, c, e0, e1);
+          const uint32_t pp = pack_bf16x2(e0, e1);
+          pk[(c / 2) % 32] = pp;
+          se2[(c / 2) & 3] = add2(se2[(c / 2) & 3], pk2(e0, e1));
+          sr2[(c / 2) & 3] = add2(sr2[(c / 2) & 3], pk2(__uint_as_float(pp << 16), __uint_as_float(pp & 0xFFFF0000u)));
+        }
+        tmem_st32(tm_s + 32 * half, pk);
+        if (half == 0) {
+          // the rescale factor goes to the correction warpgroup with the
+          // first half of P, so that it may act as soon as that is signalled
+          sh.st_scale()[t * kBM + r_in_tile] = factor;
+          const unsigned any = __any_sync(0xffffffffu, rescaled);
+          if (lane == 0) sh.warp_flag()[t * 4 + wq] = any ? 1 : 0;
+          if (p.split_p) {
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(sh.p_lo(t));
+          }
+        }
       }
       float a0, a1, b0, b1;
       up2(add2(add2(se2[0], se2[1]), add2(se2[2], se2[3])), a0, a1);
       up2(add2(add2(sr2[0], sr2[1]), add2(sr2[2], sr2[3])), b0, b1);
       l_run = l_run * factor + (a0 + a1);
       lr_run = lr_run * factor + (b0 + b1);
-      tmem_st32(tm_s + 0, pk[0]);      // P over the first 64 columns of S
-      tmem_st32(tm_s + 32, pk[1]);
       tmem_st_wait();
-      sh.st_scale()[t * kBM + r_in_tile] = factor;
-      const unsigned any = __any_sync(0xffffffffu, rescaled);
-      if (lane == 0) sh.warp_flag()[t * 4 + wq] = any ? 1 : 0;
-      if (j == w.n - 1) {
+      if (j == nt - 1) {
         sh.st_l()[t * kBM + r_in_tile] = l_run;
         sh.st_lr()[t * kBM + r_in_tile] = lr_run;
         sh.st_m()[t * kBM + r_in_tile] = m_run;
       }
       tc_fence_before();
-      mbar_arrive(sh.p_ready(t));
+      if (!p.split_p) mbar_arrive(sh.p_lo(t));
+      mbar_arrive(sh.p_hi(t));
     }
   }
 }
@@ -381,53 +433,67 @@ __device__ void correction_role(const Shared<D, VARLEN>& sh, const uint32_t tmem
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
   const int total_tok = VARLEN ? ps.header[2] : p.B * p.Sq;
   __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(p.o);
-  uint32_t sit = 0, uit = 0;
+  // phase counters per tile: a tile takes part only in the blocks it sees
+  uint32_t sit[2] = {0u, 0u}, uit[2] = {0u, 0u};
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
-    if (w.n > 0) {
-      for (int j = 0; j < w.n; ++j, ++sit) {
+    float fin_l[2] = {0.0f, 0.0f}, fin_lr[2] = {0.0f, 0.0f}, fin_m[2] = {-INFINITY, -INFINITY};
+    for (int j = 0; j < w.n; ++j) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait_bounded(sh.p_ready(t), sit & 1, sh.abort(), &g_err, kSiteCorrP, p.wait_limit_ns)) return;
-          tc_fence_after();
-          if (j > 0 && sh.warp_flag()[t * 4 + wq]) {
-            const float f = sh.st_scale()[t * kBM + r_in_tile];
-            const uint32_t tm_o = tmem + lane_off + uint32_t(256 + t * D);
+      for (int t = 0; t < 2; ++t) {
+        if (j >= w.nt[t]) continue;
+        const uint32_t ph = sit[t] & 1;
+        ++sit[t];
+        if (!mbar_wait_bounded(sh.p_lo(t), ph, sh.abort(), &g_err, kSiteCorrP, p.wait_limit_ns)) return;
+        tc_fence_after();
+        if (j > 0 && sh.warp_flag()[t * 4 + wq]) {
+          const float f = sh.st_scale()[t * kBM + r_in_tile];
+          const uint32_t tm_o = tmem + lane_off + uint32_t(256 + t * D);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tm_o + c * 32, r);
-              tmem_ld_wait();
-              tmem_ld_fence(r);
-              const uint64_t f2 = pk2(f, f);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tm_o + c * 32, r);
+            tmem_ld_wait();
+            tmem_ld_fence(r);
+            const uint64_t f2 = pk2(f, f);
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                float y0, y1;
-                up2(mul2(pk2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), f2), y0, y1);
-                r[i] = __float_as_uint(y0);
-                r[i + 1] = __float_as_uint(y1);
-              }
-              tmem_st32(tm_o + c * 32, r);
+            for (int i = 0; i < 32; i += 2) {
+              float y0, y1;
+              up2(mul2(pk2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), f2), y0, y1);
+              r[i] = __float_as_uint(y0);
+              r[i + 1] = __float_as_uint(y1);
             }
-            tmem_st_wait();
+            tmem_st32(tm_o + c * 32, r);
           }
-          tc_fence_before();
-          mbar_arrive(sh.o_ready(t));
+          tmem_st_wait();
         }
+        // The row statistics of the tile are written with the second half
+        // of P of its last block: wait for it and take them into registers
+        // before O is released (after that, the next unit's softmax may
+        // overwrite them; and waiting before o_ready keeps this barrier
+        // from running a phase ahead of the wait).
+        if (j == w.nt[t] - 1) {
+          if (!mbar_wait_bounded(sh.p_hi(t), ph, sh.abort(), &g_err, kSiteCorrP, p.wait_limit_ns)) return;
+          fin_l[t] = sh.st_l()[t * kBM + r_in_tile];
+          fin_lr[t] = sh.st_lr()[t * kBM + r_in_tile];
+          fin_m[t] = sh.st_m()[t * kBM + r_in_tile];
+        }
+        tc_fence_before();
+        mbar_arrive(sh.o_ready(t));
       }
     }
-    // epilogue: O / l in BF16, LSE in natural log
+    // epilogue: O / l in BF16, LSE in natural log (a tile that sees no key
+    // writes O = 0 and LSE = -inf for its valid rows)
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int row = w.pair * kPairRows + t * kBM + r_in_tile;
       const bool valid = row < w.seq_q;
-      float l = 0.0f, lr = 0.0f, m = -INFINITY;
-      if (w.n > 0) {
-        if (!mbar_wait_bounded(sh.o_full(t), uit & 1, sh.abort(), &g_err, kSiteCorrO, p.wait_limit_ns)) return;
+      const bool has = w.nt[t] > 0;
+      const float l = fin_l[t], lr = fin_lr[t], m = fin_m[t];
+      if (has) {
+        if (!mbar_wait_bounded(sh.o_full(t), uit[t] & 1, sh.abort(), &g_err, kSiteCorrO, p.wait_limit_ns)) return;
+        ++uit[t];
         tc_fence_after();
-        l = sh.st_l()[t * kBM + r_in_tile];
-        lr = sh.st_lr()[t * kBM + r_in_tile];
-        m = sh.st_m()[t * kBM + r_in_tile];
       }
       const float inv = (lr > 0.0f) ? 1.0f / lr : 0.0f;
       const size_t tok = size_t(w.q_tok0) + size_t(row);
@@ -436,7 +502,7 @@ __device__ void correction_role(const Shared<D, VARLEN>& sh, const uint32_t tmem
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        if (w.n > 0) {
+        if (has) {
           tmem_ld32(tm_o + c * 32, r);
           tmem_ld_wait();
           tmem_ld_fence(r);
@@ -462,10 +528,7 @@ __device__ void correction_role(const Shared<D, VARLEN>& sh, const uint32_t tmem
                                  : (size_t(w.b) * p.Hq + w.h) * p.Sq + size_t(row);
         p.lse[li] = lse;
       }
-    }
-    if (w.n > 0) {
-      tc_fence_before();
-      ++uit;
+      if (has) tc_fence_before();
     }
   }
 }
@@ -482,11 +545,11 @@ FA_DEV void s_steps(uint32_t d_tmem, uint32_t alo, uint32_t ahi, uint32_t blo, u
 }
 // Unrolled K steps of O += P V: step kk takes TMEM columns 8*kk.. of P and
 // key rows 16*kk.. of V (2048 bytes = 128 descriptor units further).
-template <int KK>
+template <int KK, int KEND>
 FA_DEV void pv_steps(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t bhi, uint32_t idesc, uint32_t acc) {
-  if constexpr (KK < kBN / 16) {
+  if constexpr (KK < KEND) {
     mma_ts_w<KK * 8, KK * 128>(d_tmem, a_tmem, blo, bhi, idesc, KK > 0 ? 1u : acc);
-    pv_steps<KK + 1>(d_tmem, a_tmem, blo, bhi, idesc, acc);
+    pv_steps<KK + 1, KEND>(d_tmem, a_tmem, blo, bhi, idesc, acc);
   }
 }
 
@@ -503,7 +566,9 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
   constexpr uint32_t kIdPV = idesc_bf16_f32(kBM, D, false, true);
   const uint32_t q_base = sh.sbase + L::kQ;
   const uint32_t kv_base = sh.sbase + L::kKV;
-  uint32_t kv_it = 0, sit = 0, uit = 0;
+  uint32_t uit = 0;
+  uint32_t sit[2] = {0u, 0u};   // phase counters per tile
+  RingPos kv{0, 0u};            // next K/V tile to consume
 
   // S_t = Q_t K^T : M = 128 rows, N = 128 keys, K = D in steps of 16.  The
   // descriptors of the 16-wide K steps differ from the first only in the
@@ -516,14 +581,28 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
   // O_t (+)= P_t V : M = 128 rows, N = D, K = 128 keys in steps of 16;
   // P from TMEM (8 columns per 16 keys), V MN-major (64-wide D chunks;
   // 16 keys = 16 rows of 128 B = 2048 B further into the V tile)
-  auto issue_pv = [&](int t, int stage, bool acc) {
+  // Keys 0-63 once the correction warpgroup has released O (it has seen
+  // the first half of P), keys 64-127 once the second half is signalled.
+  // Without split_p the correction warpgroup released O only after all of
+  // P was signalled, so the second half needs no wait of its own.
+  auto issue_pv = [&](int t, int stage, bool acc, uint32_t ph) -> bool {
     const uint64_t db = sdesc_sw128(kv_base + stage * L::kTileBytes, L::kChunkBytes, 1024);
-    pv_steps<0>(tmem + 256 + t * D, tmem + t * kBN, desc_lo(db), desc_hi(db), kIdPV, acc ? 1u : 0u);
+    pv_steps<0, 4>(tmem + 256 + t * D, tmem + t * kBN, desc_lo(db), desc_hi(db), kIdPV, acc ? 1u : 0u);
+    if (p.split_p) {
+      if (!mbar_wait_bounded(sh.p_hi(t), ph, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return false;
+      tc_fence_after();
+    }
+    pv_steps<4, 8>(tmem + 256 + t * D, tmem + t * kBN, desc_lo(db), desc_hi(db), kIdPV, 1u);
+    return true;
   };
-  auto wait_kv = [&](uint32_t it) -> bool {
-    const int stage = it % L::kStages;
-    if (!mbar_wait_bounded(sh.kv_full(stage), (it / L::kStages) & 1, sh.abort(), &g_err, kSiteMmaKV,
-                           p.wait_limit_ns))
+  const int stages = p.stages;
+  auto take_kv = [&]() {
+    const RingPos r = kv;
+    kv = ring_next(kv, stages);
+    return r;
+  };
+  auto wait_kv = [&](RingPos r) -> bool {
+    if (!mbar_wait_bounded(sh.kv_full(r.stage), r.phase, sh.abort(), &g_err, kSiteMmaKV, p.wait_limit_ns))
       return false;
     tc_fence_after();
     return true;
@@ -532,45 +611,63 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
     if (w.n == 0) continue;
+    const int n0 = w.nt[0], n1 = w.nt[1];
     if (!mbar_wait_bounded(sh.q_full(), uit & 1, sh.abort(), &g_err, kSiteMmaQ, p.wait_limit_ns)) return;
     tc_fence_after();
-    // prologue: S of both tiles for block 0
-    uint32_t k_it = kv_it++;
-    if (!wait_kv(k_it)) return;
-    issue_s(0, k_it % L::kStages);
-    mma_commit_w(sh.s_full(0));
-    issue_s(1, k_it % L::kStages);
-    mma_commit_w(sh.s_full(1));
-    mma_commit_w(sh.kv_empty(k_it % L::kStages));
+    // prologue: S of both tiles for block 0 (a tile that sees no key is
+    // skipped throughout)
+    RingPos kp = take_kv();
+    if (!wait_kv(kp)) return;
+    if (n0 > 0) {
+      issue_s(0, kp.stage);
+      mma_commit_w(sh.s_full(0));
+    }
+    if (n1 > 0) {
+      issue_s(1, kp.stage);
+      mma_commit_w(sh.s_full(1));
+    }
+    mma_commit_w(sh.kv_empty(kp.stage));
     if (w.n == 1) mma_commit_w(sh.q_empty());
-    for (int j = 0; j < w.n; ++j, ++sit) {
-      const uint32_t v_it = kv_it++;
-      if (!wait_kv(v_it)) return;
+    for (int j = 0; j < w.n; ++j) {
+      const RingPos vp = take_kv();
+      if (!wait_kv(vp)) return;
       const bool more = j + 1 < w.n;
-      if (more) k_it = kv_it++;
-      // tile 0: PV(j), then S(j+1)
-      if (!mbar_wait_bounded(sh.o_ready(0), sit & 1, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return;
-      tc_fence_after();
-      issue_pv(0, v_it % L::kStages, j > 0);
-      if (more) {
-        if (!wait_kv(k_it)) return;
-        issue_s(0, k_it % L::kStages);
-        mma_commit_w(sh.s_full(0));
-      } else {
-        mma_commit_w(sh.o_full(0));
+      bool k_ready = false;
+      if (more) kp = take_kv();
+      // tile 0: PV(j), then S(j+1) if it sees block j + 1
+      if (j < n0) {
+        const uint32_t ph = sit[0] & 1;
+        ++sit[0];
+        if (!mbar_wait_bounded(sh.o_ready(0), ph, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return;
+        tc_fence_after();
+        if (!issue_pv(0, vp.stage, j > 0, ph)) return;
+        if (j + 1 < n0) {
+          if (!wait_kv(kp)) return;
+          k_ready = true;
+          issue_s(0, kp.stage);
+          mma_commit_w(sh.s_full(0));
+        } else {
+          mma_commit_w(sh.o_full(0));
+        }
       }
-      // tile 1: PV(j), then S(j+1)
-      if (!mbar_wait_bounded(sh.o_ready(1), sit & 1, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return;
-      tc_fence_after();
-      issue_pv(1, v_it % L::kStages, j > 0);
-      mma_commit_w(sh.kv_empty(v_it % L::kStages));
+      // tile 1: PV(j), then S(j+1) if it sees block j + 1
+      if (j < n1) {
+        const uint32_t ph = sit[1] & 1;
+        ++sit[1];
+        if (!mbar_wait_bounded(sh.o_ready(1), ph, sh.abort(), &g_err, kSiteMmaO, p.wait_limit_ns)) return;
+        tc_fence_after();
+        if (!issue_pv(1, vp.stage, j > 0, ph)) return;
+        if (j + 1 == n1) mma_commit_w(sh.o_full(1));
+      }
+      mma_commit_w(sh.kv_empty(vp.stage));
       if (more) {
-        issue_s(1, k_it % L::kStages);
-        mma_commit_w(sh.s_full(1));
-        mma_commit_w(sh.kv_empty(k_it % L::kStages));
+        if (j + 1 < n1) {
+          if (!k_ready && !wait_kv(kp)) return;
+          issue_s(1, kp.stage);
+          mma_commit_w(sh.s_full(1));
+        }
+        mma_commit_w(sh.kv_empty(kp.stage));
         if (j + 1 == w.n - 1) mma_commit_w(sh.q_empty());
-      } else {
-        mma_commit_w(sh.o_full(1));
       }
     }
     ++uit;
@@ -584,7 +681,8 @@ __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq
                               const CUtensorMap* tv, const FwdParams& p, const PackedSched& ps,
                               const int total_units) {
   using L = Layout<D, VARLEN>;
-  uint32_t kv_it = 0, uit = 0;
+  uint32_t uit = 0;
+  RingPos kv{0, 0u};   // next K/V tile to fill
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
     if (w.n == 0) continue;
@@ -600,16 +698,15 @@ __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq
     for (int j = 0; j < w.n; ++j) {
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const int stage = kv_it % L::kStages;
-        if (!mbar_wait_bounded(sh.kv_empty(stage), ((kv_it / L::kStages) & 1) ^ 1, sh.abort(), &g_err,
-                               kSiteProdKV, p.wait_limit_ns))
+        const int stage = kv.stage;
+        if (!mbar_wait_bounded(sh.kv_empty(stage), kv.phase ^ 1u, sh.abort(), &g_err, kSiteProdKV, p.wait_limit_ns))
           return;
         mbar_arrive_expect_tx(sh.kv_full(stage), L::kTileBytes);
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(sh.sbase + L::kKV + stage * L::kTileBytes + c * L::kChunkBytes, which ? tv : tk,
                       sh.kv_full(stage), c * 64, hk, w.k_tok0 + j * kBN);
-        ++kv_it;
+        kv = ring_next(kv, p.stages);
       }
     }
     ++uit;
@@ -631,14 +728,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(sh.q_full(), 1);
     mbar_init(sh.q_empty(), 1);
-    for (int s = 0; s < L::kStages; ++s) {
+    for (int s = 0; s < L::kMaxStages; ++s) {
       mbar_init(sh.kv_full(s), 1);
       mbar_init(sh.kv_empty(s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(sh.s_full(t), 1);
-      mbar_init(sh.p_ready(t), kBM);
-      mbar_init(sh.o_ready(t), kBM);
+      mbar_init(sh.p_lo(t), kBM);      // one arrival per softmax thread
+      mbar_init(sh.p_hi(t), kBM);
+      mbar_init(sh.o_ready(t), kBM);   // one per correction thread
       mbar_init(sh.o_full(t), 1);
     }
     st_shared(sh.abort(), 0);
@@ -699,7 +797,8 @@ fa_status launch_inst(const FwdLaunch& L, const CUtensorMap& tq, const CUtensorM
                       cudaStream_t stream) {
   using Lay = Layout<D, VARLEN>;
   auto kern = fwd_kernel<D, CAUSAL, VARLEN, EMU>;
-  const fa_status st = prepare_kernel(reinterpret_cast<const void*>(kern), Lay::kDynamic);
+  if (L.p.stages < 2 || L.p.stages > Lay::kMaxStages) return FA_ERR_INVALID_ARG;
+  const fa_status st = prepare_kernel(reinterpret_cast<const void*>(kern), Lay::kMaxDynamic);
   if (st != FA_OK) return st;
   int grid = L.num_sms;
   if (!VARLEN) {
@@ -707,7 +806,7 @@ fa_status launch_inst(const FwdLaunch& L, const CUtensorMap& tq, const CUtensorM
     if (units < grid) grid = (int)units;
   }
   if (grid < 1) grid = 1;
-  kern<<<grid, kThreads, Lay::kDynamic, stream>>>(tq, tk, tv, L.p);
+  kern<<<grid, kThreads, Lay::dynamic_bytes(L.p.stages), stream>>>(tq, tk, tv, L.p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -24,6 +24,9 @@ struct FwdParams {
   int group;               // Hq / Hkv
   float scale_log2;        // scale * log2(e)
   float thr;               // lazy-rescale threshold in log2 units
+  int stages;              // K/V ring depth (2 .. the kernel's maximum)
+  int split_p;             // 1: each half of P (64 keys) is signalled to the MMA warp on its own
+  int sched_group;         // dense causal: (batch, head) pairs per group of the longest-first unit order
   unsigned long long wait_limit_ns;
 };
 

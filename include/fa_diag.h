@@ -27,15 +27,37 @@ extern "C" {
  *                      exponential (same page, bullet "Software
  *                      exponentials", which uses 10-25%): 0, 2, 3 or 4.
  *                      Negative selects the library default.
+ *   split_p            1: the weights P of each 128-key block are handed to
+ *                      the tensor cores in two halves of 64 keys, each on its
+ *                      own signal, so the product with V over the first half
+ *                      starts while the second half is still being computed
+ *                      ("FlashAttention-4: matrix throughput bottlenecks",
+ *                      lecompute.fr, section "Keep tiles moving without
+ *                      overwriting live data"); 0: one signal once all of P
+ *                      is written.  Negative selects the library default.
+ *   kv_stages          Depth of the K/V ring in shared memory: 2 .. 4 for
+ *                      D = 128, 2 .. 10 for D = 64.  0 or negative selects
+ *                      the library default.
+ *   head_group         Dense layout under a causal mask: the work units
+ *                      (pairs of 128-row query tiles) run longest first
+ *                      ("FlashAttention-4: Algorithm and Kernel Pipelining
+ *                      Co-Design ...", the paragraph on longest-first
+ *                      scheduling) within groups of this many (batch, head)
+ *                      pairs, group after group; B * Hq orders all heads
+ *                      together.  0 or negative selects the library default.
  */
 typedef struct {
   float rescale_threshold;
   int emu_per_16;
+  int split_p;
+  int kv_stages;
+  int head_group;
 } fa_fwd_tuning;
 
-/* The defaults fa_fwd() uses.  emu_per_16 is -1 there: the library picks
- * per configuration (2 of 16 for causal D = 128, where it measured 3% faster
- * on GB300; 0 otherwise). */
+/* The defaults fa_fwd() uses.  emu_per_16, split_p, kv_stages and
+ * head_group are -1 there: the library picks them per configuration (head
+ * dimension, causal mask, sequence length) from a table of measured
+ * choices. */
 FA_API fa_fwd_tuning fa_fwd_default_tuning(void);
 
 /* fa_fwd() with explicit knobs; `t` may be NULL for the defaults. */

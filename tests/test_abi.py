@@ -70,10 +70,15 @@ def test_forward_rejects_bad_arguments(lib, kw, status):
 def test_forward_tuning_validation(lib):
     from exact_attention_78_gb300.binding import FwdTuning
     t = lib.fa_fwd_default_tuning()
-    assert t.rescale_threshold == 8.0 and t.emu_per_16 in (-1, 0, 2, 3, 4)
-    for thr, emu in ((-1.0, 0), (17.0, 0), (8.0, 1), (8.0, 5), (float("nan"), 0)):
-        bad = FwdTuning(thr, emu)
+    assert t.rescale_threshold == 8.0 and t.emu_per_16 == -1 and t.split_p == -1 and t.kv_stages == -1
+    assert t.head_group == -1
+    for thr, emu, split, stages in ((-1.0, 0, -1, -1), (17.0, 0, -1, -1), (8.0, 1, -1, -1), (8.0, 5, -1, -1),
+                                    (float("nan"), 0, -1, -1), (8.0, 0, 2, -1), (8.0, 0, 0, 1), (8.0, 0, 0, 5)):
+        bad = FwdTuning(thr, emu, split, stages, -1)
         assert lib.fa_fwd_ex(A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, 0.125, None, ctypes.byref(bad), None) == 1
+    # D = 64 allows a deeper ring than D = 128
+    bad = FwdTuning(8.0, 0, 0, 11, -1)
+    assert lib.fa_fwd_ex(A, A, A, A, A, 1, 2, 2, 128, 128, 64, 0, 0.125, None, ctypes.byref(bad), None) == 1
 
 
 def _ws(lib, B, Hq, Hkv, Sq, Sk, D, det, total_q=0, offs=None):

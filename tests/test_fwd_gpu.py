@@ -12,7 +12,8 @@ import torch
 
 from exact_attention_78_gb300 import workloads as W
 
-from parity import LSE_ATOL, O_ATOL, check_forward_full, check_forward_sampled, f64
+import oracle
+from parity import LSE_ATOL, O_ATOL, check_forward_full, check_forward_sampled, f64, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -79,21 +80,40 @@ def test_causal_first_row_equals_first_value(fa):
     np.testing.assert_allclose(f64(o)[:, 0], f64(v)[:, 0], atol=8e-3)
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_lazy_equals_eager_under_stress(fa, causal):
-    """Q x 4 (logit std ~16): running maxima keep growing.  Lazy (threshold 8)
-    and eager (threshold 0) rescaling agree up to rounding, and both match
-    the oracle.  Both runs use the hardware exponential only, so that the
-    comparison isolates the rescaling rule (the FMA polynomial's own error
-    depends on its argument, which differs between the two rules; its
-    accuracy has its own tests)."""
-    q, k, v = _dense(1, 4, 4, 1024, 1024, 128, seed=1, q_scale=4.0)
+def test_lazy_equals_eager_under_stress(fa, D, causal):
+    """Q x 4 (logit std ~16): running maxima keep growing.  Lazy rescaling
+    (threshold 8) is exact ("FlashAttention-4: Algorithm and Kernel
+    Pipelining Co-Design ...", bullet "Lazy rescaling": skipping the rescale
+    leaves the result unchanged), so it may differ from eager rescaling
+    (threshold 0) only by rounding: the weights are rounded to BF16 at a
+    different scale, and O is rounded to BF16 at the end.
+
+    Pinned here, on whole tensors:
+      * lazy and eager O differ by at most 2.5e-3 relative Frobenius (BF16
+        output rounding alone is ~1.1e-3; measured 1.3-1.7e-3) -- six times
+        tighter than the 1.5e-2 max-abs parity tolerance;
+      * at least 90% of lazy O elements are within one BF16 ulp of eager O
+        (measured 92-96%);
+      * lazy is as accurate as eager against the fp64 oracle (relative
+        Frobenius within 15%; measured ratio 1.05-1.08);
+      * LSE agrees to 1e-5 (measured 1.9e-6).
+    Both runs use the hardware exponential only, so that the comparison
+    isolates the rescaling rule (the FMA polynomial's own error depends on
+    its argument, which differs between the two rules; its accuracy has its
+    own tests)."""
+    q, k, v = _dense(1, 4, 4, 1024, 1024, D, seed=1, q_scale=4.0)
     o_l, lse_l = _run(fa, q, k, v, causal, rescale_threshold=8.0, emu_per_16=0)
     o_e, lse_e = _run(fa, q, k, v, causal, rescale_threshold=0.0, emu_per_16=0)
-    check_forward_full(o_l, lse_l, q, k, v, causal, 128 ** -0.5)
-    check_forward_full(o_e, lse_e, q, k, v, causal, 128 ** -0.5)
-    assert float((o_l.float() - o_e.float()).abs().max()) <= 1.6e-2
-    assert float((lse_l - lse_e).abs().max()) <= 2e-5
+    check_forward_full(o_l, lse_l, q, k, v, causal, D ** -0.5)
+    check_forward_full(o_e, lse_e, q, k, v, causal, D ** -0.5)
+    o_ref, _ = oracle.attention_forward(f64(q), f64(k), f64(v), causal, D ** -0.5)
+    assert rel_fro(f64(o_l), f64(o_e)) <= 2.5e-3
+    ulps = (o_l.view(torch.int16).long() - o_e.view(torch.int16).long()).abs()
+    assert float((ulps <= 1).float().mean()) >= 0.90
+    assert rel_fro(f64(o_l), o_ref) <= 1.15 * rel_fro(f64(o_e), o_ref)
+    assert float((lse_l - lse_e).abs().max()) <= 1e-5
 
 
 @pytest.mark.parametrize("emu", [0, 2, 3, 4])
@@ -101,6 +121,48 @@ def test_exp2_emulation_fraction_keeps_parity(fa, emu):
     q, k, v = _dense(2, 2, 2, 640, 640, 128, seed=3)
     o, lse = _run(fa, q, k, v, True, emu_per_16=emu)
     check_forward_full(o, lse, q, k, v, True, 128 ** -0.5)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_p_and_ring_depth_change_no_bits(fa, D, causal):
+    """P handed to the tensor cores in two halves (split_p = 1) or at once,
+    and every K/V ring depth: the same products are issued in the same order,
+    only their timing changes, so O and LSE are bitwise identical -- and
+    match the oracle."""
+    q, k, v = _dense(2, 3, 3, 700, 700, D, seed=5)
+    base_o, base_l = _run(fa, q, k, v, causal, split_p=0)
+    check_forward_full(base_o, base_l, q, k, v, causal, D ** -0.5)
+    max_stages = 4 if D == 128 else 10
+    for split in (0, 1):
+        for stages in (2, 3, max_stages):
+            o, lse = _run(fa, q, k, v, causal, split_p=split, kv_stages=stages)
+            assert torch.equal(o.view(torch.int16), base_o.view(torch.int16)), (split, stages)
+            assert torch.equal(lse, base_l), (split, stages)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_causal_head_groups_change_no_bits(fa, D):
+    """Longest-first order within groups of 1, 4 or all (batch, head) pairs:
+    each work unit computes the same thing wherever it runs."""
+    q, k, v = _dense(2, 3, 3, 900, 900, D, seed=6)
+    base_o, base_l = _run(fa, q, k, v, True, head_group=6)
+    check_forward_full(base_o, base_l, q, k, v, True, D ** -0.5)
+    for g in (1, 4, 100):
+        o, lse = _run(fa, q, k, v, True, head_group=g)
+        assert torch.equal(o.view(torch.int16), base_o.view(torch.int16)), g
+        assert torch.equal(lse, base_l), g
+
+
+@pytest.mark.parametrize("split_p", [0, 1])
+def test_split_p_packed_lengths(fa, split_p):
+    lens = [1, 130, 0, 513, 256, 77, 1000, 128, 129]
+    cu = W.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    q, k, v = W.randn_bf16((T, 4, 128), 31), W.randn_bf16((T, 2, 128), 32), W.randn_bf16((T, 2, 128), 33)
+    for causal in (False, True):
+        o, lse = _run(fa, q, k, v, causal, cu=cu, split_p=split_p)
+        check_forward_full(o, lse, q, k, v, causal, 128 ** -0.5, cu=cu)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -175,7 +237,8 @@ def test_dense_config_sampled(fa, causal, stress):
     _sampled(fa, w, [(0, 0), (1, 7), (3, 15)], rows)
 
 
-@pytest.mark.parametrize("S,D", [(1024, 64), (32768, 128)])
+@pytest.mark.parametrize("S", list(W.SWEEP_S))
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_sweep_config_sampled(fa, S, D, causal):
     w = W.sweep(S, D, causal)
