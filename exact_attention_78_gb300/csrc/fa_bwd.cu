@@ -58,6 +58,8 @@
 // [256, 384), dK [384, 512).
 #include <cuda_runtime.h>
 
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -716,12 +718,16 @@ __device__ void elementwise_role(const Shared<kD>& sh, const uint32_t tmem, cons
       int cmin = 0;
       if (key >= u_lk<PACKED>(w, p)) cmin = kBM;
       else if (p.causal) cmin = min(kBM, max(0, key - (u_lk<PACKED>(w, p) - u_lq<PACKED>(w, p)) - kBM * i));
-      const float2* nl = reinterpret_cast<const float2*>(sh.stage_nlse2(st) + kC0);
-      const float2* nd = reinterpret_cast<const float2*>(sh.stage_ndelta(st) + kC0);
+      // row terms of the 32 columns: 16-byte broadcast loads (every lane
+      // reads the same address), four columns per shared-memory wavefront
+      const float4* nl = reinterpret_cast<const float4*>(sh.stage_nlse2(st) + kC0);
+      const float4* nd = reinterpret_cast<const float4*>(sh.stage_ndelta(st) + kC0);
       uint32_t pp[16], dd[16];
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
-        const float2 l2 = nl[c / 2], d2 = nd[c / 2];
+        const float4 l4 = nl[c / 4], d4 = nd[c / 4];
+        const float2 l2 = (c & 2) ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y);
+        const float2 d2 = (c & 2) ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
         const uint64_t x = fma2(pk2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, pk2(l2.x, l2.y));
         float x0, x1;
         up2(x, x0, x1);
@@ -1137,21 +1143,61 @@ namespace bwd {
 static __device__ __align__(256) unsigned char g_static_scratch[FA_BWD_STATIC_SCRATCH_BYTES];
 }
 
-// Device address of the buffer on the current device, looked up once per
-// device (the symbol's host-side name is not a device address).
+// Device address of the buffer in the current CUDA context.  The symbol's
+// host-side name is not a device address, and the address belongs to the
+// context that loaded the module: it is looked up once per context (with that
+// context current) and cached under the context's unique id, so that a
+// context created later (after cudaDeviceReset, or a non-primary context made
+// current by the caller) gets its own lookup instead of a stale address.
+static CUresult current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  if (!get_current || !get_id) return CUDA_ERROR_NOT_FOUND;
+  CUcontext ctx = nullptr;
+  const CUresult r = get_current(&ctx);
+  if (r != CUDA_SUCCESS) return r;
+  if (ctx == nullptr) return CUDA_ERROR_INVALID_CONTEXT;
+  return get_id(ctx, id);
+}
+
 static fa_status static_scratch_address(void** out) {
-  constexpr int kMaxDevices = 64;
-  static void* addr[kMaxDevices] = {};
+  constexpr int kMaxContexts = 64;
+  static unsigned long long ids[kMaxContexts] = {};
+  static void* addr[kMaxContexts] = {};
+  static int n = 0;
   static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, bwd::g_static_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
-    addr[dev] = p;
+  unsigned long long id = 0;
+  if (current_context_id(&id) == CUDA_SUCCESS) {
+    for (int i = 0; i < n; ++i)
+      if (ids[i] == id) {
+        *out = addr[i];
+        return FA_OK;
+      }
   }
-  *out = addr[dev];
+  // first call in this context (the lookup also initialises the runtime's
+  // context when none is current yet)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, bwd::g_static_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+  if (current_context_id(&id) != CUDA_SUCCESS) return FA_ERR_CUDA;
+  if (n < kMaxContexts) {
+    ids[n] = id;
+    addr[n] = p;
+    ++n;
+  }
+  *out = p;
   return FA_OK;
 }
 

@@ -141,9 +141,11 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
  *   - Needs no more than fa_bwd_workspace_size(...) <= 64 MiB (for example
  *     B * Sq * Hq * D * 4 bytes of dQ accumulator); larger problems are
  *     rejected with FA_ERR_WORKSPACE before anything is launched.
- *   - Allocates nothing.  The first call on a device looks up the buffer's
- *     device address (cudaGetSymbolAddress) with that device current; make
- *     that first call before any stream capture.
+ *   - Allocates nothing.  The first call on a device (more exactly, in each
+ *     CUDA context: again after cudaDeviceReset or in a context the caller
+ *     created) looks up the buffer's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream
+ *     capture.
  *   - All calls share the one buffer and it keeps the last call's contents;
  *     the call clears what must start at zero itself.  Calls whose work
  *     overlaps on the GPU (other streams, other host threads) race on the

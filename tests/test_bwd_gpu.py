@@ -153,3 +153,49 @@ def test_training_shape_sampled_heads(fa, deterministic):
         for name, g, r in (("dq", dq[b, :, h], gq), ("dk", dk[b, :, h], gk), ("dv", dv[b, :, h], gv)):
             e = rel_fro(f64(g), r)
             assert e <= GRAD_RTOL, (b, h, name, e)
+
+
+def _heads_vs_oracle(q, k, v, do, grads, causal, scale, heads):
+    """Whole (batch, head) slices of the gradients against the oracle's
+    analytic gradients of that head (Hq == Hkv)."""
+    dq, dk, dv = grads
+    worst = 0.0
+    for b, h in heads:
+        gq, gk, gv = oracle.head_backward(f64(q[b, :, h]), f64(k[b, :, h]), f64(v[b, :, h]), f64(do[b, :, h]),
+                                          causal, scale)
+        for name, g, r in (("dq", dq[b, :, h], gq), ("dk", dk[b, :, h], gk), ("dv", dv[b, :, h], gv)):
+            e = rel_fro(f64(g), r)
+            worst = max(worst, e)
+            assert e <= GRAD_RTOL, (b, h, name, e)
+    return worst
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("stress", [False, True])
+def test_dense_config_sampled_heads(fa, causal, stress):
+    """The benchmark's dense workload (B=4, H=16, S=4096, D=128) at full size,
+    through fa_bwd's default launch (static schedule: head-major without a
+    mask, key-block-major within groups of 32 heads with one), so every CTA
+    runs many units.  Whole heads spread over the batch and the head range
+    are compared; the Q x 4 stress seed (logit std ~16) exercises large
+    maxima in the recomputed weights."""
+    w = W.dense(causal=causal, stress=stress)
+    (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
+    grads = _gpu_grads(fa, q, k, v, do, causal)
+    for t in grads:
+        assert bool(torch.isfinite(t.float()).all())
+    _heads_vs_oracle(q, k, v, do, grads, causal, w.scale, [(0, 0), (1, 9), (3, 15)])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("S", [1024, 2048, 4096, 8192])
+@pytest.mark.parametrize("causal", [False, True])
+def test_sweep_config_sampled_heads(fa, D, S, causal):
+    """Sequence-length sweep (B*S = 32768 tokens, H=16) at full size: the
+    first and the last (batch, head) slice of each call."""
+    w = W.sweep(S, D, causal)
+    (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
+    grads = _gpu_grads(fa, q, k, v, do, causal)
+    for t in grads:
+        assert bool(torch.isfinite(t.float()).all())
+    _heads_vs_oracle(q, k, v, do, grads, causal, w.scale, [(0, 0), (w.B - 1, 15)])

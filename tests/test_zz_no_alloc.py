@@ -56,6 +56,39 @@ def test_noalloc_backward_matches_fa_bwd_twice(deterministic):
                 assert torch.equal(g.view(torch.int16), r.view(torch.int16)), (call, name)
 
 
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_noalloc_packed_backward_matches_fa_bwd_twice(deterministic):
+    """Packed variable-length layout with grouped heads: here the built-in
+    buffer also holds the per-sequence tables and the work order that the
+    first kernel writes, so two calls in a row show that none of the earlier
+    call's contents leaks into the next."""
+    import exact_attention_78_gb300 as fa
+    lib = fa.load_library(build_if_missing=True)
+    lens = [300, 1, 700, 129, 0, 256]
+    cu = W.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    Hq, Hkv, D = 4, 2, 128
+    assert fa.bwd_workspace_size(len(lens), Hq, Hkv, T, T, D, deterministic, total_q=T) <= STATIC_SCRATCH_BYTES
+    q, k, v, do = (W.randn_bf16((T, h, D), 40 + i).cuda() for i, h in enumerate((Hq, Hkv, Hkv, Hq)))
+    cud = cu.cuda()
+    o, lse = fa.fwd(q, k, v, causal=True, cu_seqlens=cud)
+    ref = fa.bwd(q, k, v, o, lse, do, causal=True, deterministic=deterministic, cu_seqlens=cud)
+    assert fa.get_device_error() == 0
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    for call in range(2):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        st = lib.fa_bwd_noalloc(p(q), p(k), p(v), p(o), p(lse), p(do), p(dq), p(dk), p(dv), len(lens), Hq, Hkv,
+                                T, T, D, 1, D ** -0.5, p(cud), int(deterministic),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0, (call, st)
+        assert fa.get_device_error() == 0
+        for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            e = rel_fro(f64(g), f64(r))
+            assert e <= GRAD_RTOL, (call, name, e)
+            if deterministic:
+                assert torch.equal(g.view(torch.int16), r.view(torch.int16)), (call, name)
+
+
 def test_noalloc_rejects_problems_larger_than_its_buffer():
     import exact_attention_78_gb300 as fa
     lib = fa.load_library(build_if_missing=True)
