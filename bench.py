@@ -57,9 +57,15 @@ def parse():
     ap.add_argument("--S", type=int, default=4096)
     ap.add_argument("--D", type=int, default=128)
     ap.add_argument("--emu", type=int, default=None, help="exp2 emulation: entries of every 16 on FMA")
+    ap.add_argument("--fwd-tune", default="",
+                    help="forward knobs as name=value,... (split_p, kv_stages, head_group); "
+                         "default: the library's per-configuration choice")
     ap.add_argument("--bwd-tune", default="",
                     help="backward knobs as name=value,... (schedule, head_group, reverse_blocks, scores_first); "
                          "default: the library's per-call choice")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="repeat the block of --steps timed steps until the blocks together last this long "
+                         "(so that clock samples see the GPU under load); the median block is reported")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline sample")
     return ap.parse_args()
@@ -273,6 +279,9 @@ def run_gpu(args):
     det = bool(w.extra.get("deterministic", args.deterministic))
     paired = True if args.paired else None
     tuning = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.bwd_tune.split(",") if kv} or None
+    fwd_knobs = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.fwd_tune.split(",") if kv}
+    if args.emu is not None:
+        fwd_knobs["emu_per_16"] = args.emu
 
     have_bwd = not args.fwd_only
     ws_buf = dq = dk = dv = None
@@ -286,7 +295,7 @@ def run_gpu(args):
             need = fa.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, det)
         ws_buf = torch.empty(need, dtype=torch.uint8, device="cuda")
         dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-        fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, emu_per_16=args.emu)
+        fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, **fwd_knobs)
         fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal, deterministic=det, workspace=ws_buf, dq=dq, dk=dk,
                dv=dv, paired=paired, cu_seqlens=cud, tuning=tuning)
     torch.cuda.synchronize()
@@ -294,11 +303,12 @@ def run_gpu(args):
     ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_b1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    fwd_times, bwd_times = [], []
 
     def step(i=None):
         if i is not None:
             ev_f0[i].record(stream)
-        fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, emu_per_16=args.emu)
+        fa.fwd(qd, kd, vd, causal=w.causal, cu_seqlens=cud, out=o, lse=lse, **fwd_knobs)
         if i is not None:
             ev_f1[i].record(stream)
         if have_bwd:
@@ -318,20 +328,37 @@ def run_gpu(args):
         replicas.barrier()
         torch.cuda.synchronize()
 
+    # Timed region: blocks of exactly `steps` steps, each bracketed by a
+    # barrier and a device synchronisation on both sides and timed with CUDA
+    # events on the launching stream.  A block of a few milliseconds is too
+    # short for clock samples taken every 100 ms to see the GPU under load,
+    # so blocks repeat until together they last --min-timed-s; the median
+    # block (max over ranks) is reported, and the per-call times average
+    # over every timed step.
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    block_ms = []
+    max_blocks = 1000
     with ClockSampler(local) as clocks:
-        start.record(stream)
-        for i in range(args.steps):
-            step(i)
-        end.record(stream)
-        torch.cuda.synchronize()
-    barrier()
+        while True:
+            barrier()
+            start.record(stream)
+            for i in range(args.steps):
+                step(i)
+            end.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            block_ms.append(replicas.max_over_ranks(start.elapsed_time(end), device="cuda"))
+            fwd_times += [ev_f0[i].elapsed_time(ev_f1[i]) for i in range(args.steps)]
+            if have_bwd:
+                bwd_times += [ev_f1[i].elapsed_time(ev_b1[i]) for i in range(args.steps)]
+            # every rank takes the same decision (block times are already the max over ranks)
+            if sum(block_ms) >= args.min_timed_s * 1e3 or len(block_ms) >= max_blocks:
+                break
     if fa.get_device_error() != 0:
         raise RuntimeError("device error in timed region")
-    elapsed_ms = replicas.max_over_ranks(start.elapsed_time(end), device="cuda")
-    fwd_ms = statistics.mean(ev_f0[i].elapsed_time(ev_f1[i]) for i in range(args.steps))
-    bwd_ms = statistics.mean(ev_f1[i].elapsed_time(ev_b1[i]) for i in range(args.steps)) if have_bwd else 0.0
+    elapsed_ms = statistics.median(block_ms)
+    fwd_ms = statistics.mean(fwd_times)
+    bwd_ms = statistics.mean(bwd_times) if have_bwd else 0.0
 
     flops_step = step_flops(w, have_bwd)
     ms_step = elapsed_ms / args.steps
@@ -373,8 +400,8 @@ def run_gpu(args):
             stream.wait_event(copied[bset])
             if i >= 2:
                 stream.wait_event(read[bset])        # step i - 2's results have left
-            fa.fwd(ins[0], ins[1], ins[2], causal=w.causal, cu_seqlens=cud, out=oo, lse=ll, emu_per_16=args.emu,
-                   stream=stream)
+            fa.fwd(ins[0], ins[1], ins[2], causal=w.causal, cu_seqlens=cud, out=oo, lse=ll, stream=stream,
+                   **fwd_knobs)
             if have_bwd:
                 fa.bwd(ins[0], ins[1], ins[2], oo, ll, ins[3], causal=w.causal, deterministic=det, workspace=ws_buf,
                        dq=gg[0], dk=gg[1], dv=gg[2], paired=paired, cu_seqlens=cud, stream=stream, tuning=tuning)
@@ -419,12 +446,18 @@ def run_gpu(args):
         dom, dom_ms, dom_flops = "fwd", fwd_ms, fwd_flops_of(w)
     kname = "bwd_pair_kernel" if (dom == "bwd" and args.paired) else dom + "_kernel"
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    # Denominator: the burst BF16 peak (a dense GEMM timed for milliseconds
+    # at full clock), because each call here runs for milliseconds; the
+    # fraction of the sustained (seconds-long, power-capped) figure is given
+    # beside it for context.
+    peak = float(pk["bf16_tflops"])
+    sustained = pk.get("bf16_tflops_sustained")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": measured_traffic(kname, w), "kernel": kname,
                 "timed": ("the whole backward call (its pre, main and post kernels), CUDA events on its stream"
                           if dom == "bwd" else "the forward call (one kernel), CUDA events on its stream"),
-                "peak_kind": "%s, sustained bf16 (kernel timed inside a repeated step)" % pk_kind}
+                "peak_kind": "%s burst bf16 (bf16_tflops)" % pk_kind,
+                "frac_of_sustained": achieved / float(sustained) if sustained else None}
 
     cpu = None
     if not args.no_cpu:
@@ -437,6 +470,7 @@ def run_gpu(args):
         "config": {**w.describe(), "step": "fwd+bwd" if have_bwd else "fwd", "deterministic": det,
                    "bwd_kernel": "paired CTAs" if args.paired else "single CTA",
                    **({"bwd_tuning": tuning} if tuning else {}),
+                   **({"fwd_tuning": fwd_knobs} if fwd_knobs else {}),
                    "l2": "inputs larger than L2 (Q,K,V,O %d MiB each)" % (qd.numel() * 2 >> 20),
                    "parallelism": "replicas" if ws > 1 else "single"},
         "fwd_tflops": fwd_flops_of(w) / (fwd_ms * 1e-3) / 1e12,
@@ -446,9 +480,13 @@ def run_gpu(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        # per step: the forward kernel; the backward's pre, main and post
-        # kernels (packed layout: plus the offset-checking plan kernel)
-        "gpu_launches": args.steps * (1 + ((4 if w.packed else 3) if have_bwd else 0)),
+        # per timed step (every block): the forward kernel; the backward's
+        # pre, main and post kernels (packed layout: plus the offset-checking
+        # plan kernel)
+        "gpu_launches": len(block_ms) * args.steps * (1 + ((4 if w.packed else 3) if have_bwd else 0)),
+        "timed_blocks": {"blocks": len(block_ms), "steps_per_block": args.steps,
+                         "block_ms_min": min(block_ms), "block_ms_median": elapsed_ms,
+                         "block_ms_max": max(block_ms), "total_s": sum(block_ms) / 1e3},
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
