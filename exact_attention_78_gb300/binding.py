@@ -30,7 +30,7 @@ class FwdTuning(ctypes.Structure):
 
 class BwdTuning(ctypes.Structure):
     _fields_ = [("paired", ctypes.c_int), ("schedule", ctypes.c_int), ("head_group", ctypes.c_int),
-                ("reverse_blocks", ctypes.c_int), ("scores_first", ctypes.c_int)]
+                ("reverse_blocks", ctypes.c_int), ("scores_first", ctypes.c_int), ("split_dq", ctypes.c_int)]
 
 
 _LIB = None
@@ -190,7 +190,7 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, deterministic=False, work
     or packed [total,H,D] with cu_seqlens (LSE [Hq, total]).  paired=True runs
     the main kernel on CTA pairs (paired tcgen05 MMAs; dense only).  tuning:
     a dict of fa_bwd_tuning fields (schedule, head_group, reverse_blocks,
-    scores_first) overriding the per-call defaults."""
+    scores_first, split_dq) overriding the per-call defaults."""
     unknown = set(tuning or {}) - {f[0] for f in BwdTuning._fields_}
     if unknown:
         raise KeyError("unknown backward tuning field(s): %s" % ", ".join(sorted(unknown)))

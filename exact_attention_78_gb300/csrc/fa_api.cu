@@ -289,6 +289,7 @@ fa_bwd_tuning fa_bwd_default_tuning(void) {
   t.head_group = -1;
   t.reverse_blocks = -1;
   t.scores_first = -1;
+  t.split_dq = -1;
   return t;
 }
 
@@ -299,13 +300,15 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   try {
     fa_bwd_tuning tune = fa_bwd_default_tuning();
     if (t) {
-      if (t->paired > 1 || t->schedule > 1 || t->reverse_blocks > 1 || t->scores_first > 1 || t->head_group == 0)
+      if (t->paired > 1 || t->schedule > 1 || t->reverse_blocks > 1 || t->scores_first > 1 || t->split_dq > 1 ||
+          t->head_group == 0)
         return FA_ERR_INVALID_ARG;
       if (t->paired >= 0) tune.paired = t->paired;
       tune.schedule = t->schedule;
       tune.head_group = t->head_group;
       tune.reverse_blocks = t->reverse_blocks;
       tune.scores_first = t->scores_first;
+      tune.split_dq = t->split_dq;
     }
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
@@ -372,19 +375,23 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     // (the plan kernel writes the order; varlen GQA workload, 64 sequences:
     // groups of 8 / 16 / 32 / 64 / 512 pairs: 1013 / 1006 / 988 / 740 / 661
     // TFLOPS, deterministic 591 / - / 717 / 632 / 569).
+    // The split backward (default in deterministic mode) has no ordered
+    // additions, so its main kernel takes the schedule of the atomic mode.
+    const bool split = tune.paired != 1 && (tune.split_dq >= 0 ? tune.split_dq == 1 : deterministic == 1);
+    const bool tickets = deterministic && !split;
     {
       const long long bh = (long long)B * Hkv;
       const bool dynamic = tune.schedule >= 0 ? tune.schedule == 1 : packed;
       long long g = 1;
       if (tune.head_group > 0) g = tune.head_group;
-      else if (packed) g = deterministic ? 32 : 16;
-      else if (deterministic) g = bh;
+      else if (packed) g = tickets ? 32 : 16;
+      else if (tickets) g = bh;
       else if (causal) g = 32;
       if (g > bh) g = bh;
       L.p.sched_group = (int)g;
       L.p.sched_dynamic = dynamic ? 1 : 0;
-      L.p.rev_blocks = tune.reverse_blocks >= 0 ? tune.reverse_blocks : (deterministic ? 1 : 0);
-      L.p.scores_first = tune.scores_first >= 0 ? tune.scores_first : (deterministic ? 0 : 1);
+      L.p.rev_blocks = tune.reverse_blocks >= 0 ? tune.reverse_blocks : (tickets ? 1 : 0);
+      L.p.scores_first = tune.scores_first >= 0 ? tune.scores_first : (tickets ? 0 : 1);
     }
     L.p.B = B;
     L.p.Hq = Hq;
@@ -400,6 +407,7 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     L.p.wait_limit_ns = kDefaultWaitLimitNs;
     L.num_sms = num_sms;
     L.pair = tune.paired == 1 && !packed && D == 128;
+    L.split_dq = split;
     return launch_bwd(L, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {
     return FA_ERR_CUDA;
@@ -417,8 +425,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 fa_status fa_get_device_error(fa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   fa_status first = FA_OK;
-  const fa_status all[4] = {fwd_take_device_error(), bwd_take_device_error(), bwd_pair_take_device_error(),
-                            diag_take_device_error()};
+  const fa_status all[5] = {fwd_take_device_error(), bwd_take_device_error(), bwd_pair_take_device_error(),
+                            bwd_dq_take_device_error(), diag_take_device_error()};
   for (fa_status s : all)
     if (first == FA_OK && s != FA_OK) first = s;
   return first;

@@ -138,7 +138,8 @@ FA_DEV void zero_row_part(float* a) {
 
 // One warp per padded query row (b, h, q): stores -LSE * log2(e) and -Delta
 // (negated so the main kernel adds them with one packed FMA / ADD) and zeroes
-// the row's dQ accumulator.  Rows q >= Sq (padding) and rows that saw no key
+// the row's dQ accumulator (when there is one: the split backward writes dQ
+// from its own kernel).  Rows q >= Sq (padding) and rows that saw no key
 // (LSE = -inf) get -inf and 0, so their weights come out as exactly 0.
 template <int kD>
 __global__ void pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
@@ -165,7 +166,7 @@ __global__ void pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloa
       dl = -acc;
       const float lv = lse[(size_t(b) * Hq + h) * Sq + q];
       l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
-      zero_row_part<kD>(dq_acc + off);
+      if (dq_acc) zero_row_part<kD>(dq_acc + off);
     }
     if (lane == 0) {
       ndelta[r] = dl;
@@ -343,7 +344,7 @@ __global__ void pre_packed_kernel(const __nv_bfloat16* __restrict__ o, const __n
         dl = -acc;
         const float lv = lse[(size_t)h * total + tok];
         l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
-        zero_row_part<kD>(dq_acc + e);
+        if (dq_acc) zero_row_part<kD>(dq_acc + e);
       }
     }
     if (lane == 0) {
@@ -606,7 +607,7 @@ FA_DEV void dq_steps(uint32_t d_dq, uint32_t klo, uint32_t khi, uint32_t slo, ui
 }
 
 // MMA issuer: the whole warp runs this, converged; an elected lane issues.
-template <int kD, bool PACKED, bool DYN>
+template <int kD, bool PACKED, bool DYN, bool DQ>
 __device__ void mma_role(const Shared<kD>& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   constexpr uint32_t kIdS = idesc_bf16_f32(kBN, kBM, false, false);   // S^T, dP^T: 128 keys x 64 queries
   constexpr uint32_t kIdG = idesc_bf16_f32(kBN, kD, false, true);     // dV, dK: A in TMEM, B MN-major
@@ -632,10 +633,10 @@ __device__ void mma_role(const Shared<kD>& sh, const uint32_t tmem, const BwdPar
     const int buf = t & 1, st = t % kStages;
     const uint32_t ph = (t / kStages) & 1;
     if (!wait(sh.q_full(st), ph, kSiteMmaQ)) return false;
-    if (!p.scores_first && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
+    if (DQ && !p.scores_first && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
     const uint64_t dq = sdesc_sw128(sh.stage(st), 16, 1024);
     score_steps<kD, 0>(tmem + kColBuf * buf, desc_lo(dk_kmaj), desc_hi(dk_kmaj), desc_lo(dq), desc_hi(dq), kIdS);
-    if (p.scores_first && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
+    if (DQ && p.scores_first && !wait(sh.dq_empty(buf), ((t >> 1) & 1) ^ 1, kSiteMmaDq)) return false;
     if (!wait(sh.qd_full(st), ph, kSiteMmaQ)) return false;
     const uint64_t dg = sdesc_sw128(sh.stage(st) + Layout<kD>::kQTile, 16, 1024);
     score_steps<kD, 0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dv_kmaj), desc_hi(dv_kmaj), desc_lo(dg), desc_hi(dg),
@@ -665,14 +666,17 @@ __device__ void mma_role(const Shared<kD>& sh, const uint32_t tmem, const BwdPar
       grad_steps<0>(tmem + kColDV, tmem + kColDK, tmem + kColBuf * buf, tmem + kColBuf * buf + kColDPoff,
                     desc_lo(dgo), desc_hi(dgo), desc_lo(dqq), desc_hi(dqq), kIdG, s > 0 ? 1u : 0u);
       mma_commit_w(sh.qd_empty(st));
-      // dQ_i^T = K^T dS^T over the dP^T columns of this buffer (its dS^T has
-      // just been read by the dK product, issued before): M = D (K MN-major,
-      // chunks 16 KB apart), N = 64 queries (dS^T MN-major), K = 128 keys
-      const uint64_t dsd = sdesc_sw128(sh.ds(buf), Layout<kD>::kDsBytes, 1024);
-      dq_steps<0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd),
-                  kIdQ);
-      mma_commit_w(sh.dq_full(buf));
-      mma_commit_w(sh.ds_free(buf));
+      if constexpr (DQ) {
+        // dQ_i^T = K^T dS^T over the dP^T columns of this buffer (its dS^T
+        // has just been read by the dK product, issued before): M = D (K
+        // MN-major, chunks 16 KB apart), N = 64 queries (dS^T MN-major),
+        // K = 128 keys
+        const uint64_t dsd = sdesc_sw128(sh.ds(buf), Layout<kD>::kDsBytes, 1024);
+        dq_steps<0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dk_mn), desc_hi(dk_mn), desc_lo(dsd), desc_hi(dsd),
+                    kIdQ);
+        mma_commit_w(sh.dq_full(buf));
+        mma_commit_w(sh.ds_free(buf));
+      }
     }
     mma_commit_w(sh.acc_full());
     mma_commit_w(sh.kv_empty());
@@ -683,7 +687,7 @@ __device__ void mma_role(const Shared<kD>& sh, const uint32_t tmem, const BwdPar
 // P / dS warpgroups: thread = key row kr of the unit's key block; warpgroup
 // H handles query columns [32 H, 32 H + 32) of each 64-row step, so two
 // warpgroups (one warp per scheduler each) share the elementwise work.
-template <int kD, bool PACKED, bool DYN, int H>
+template <int kD, bool PACKED, bool DYN, bool DQ, int H>
 __device__ void elementwise_role(const Shared<kD>& sh, const uint32_t tmem, const BwdParams& p,
                                  const int total_units) {
   constexpr int kC0 = 32 * H;   // first query column of this warpgroup
@@ -748,16 +752,18 @@ __device__ void elementwise_role(const Shared<kD>& sh, const uint32_t tmem, cons
       tmem_st16(tb + kColDPoff + kC0, dd);
       // dS^T into shared memory (B operand of dQ^T): row kr, 128-byte rows,
       // 16-byte chunk j (queries 8 j .. 8 j + 7) stored at chunk j ^ (kr mod 8)
-      if (!mbar_wait_bounded(sh.ds_free(buf), ((sit >> 1) & 1) ^ 1, sh.abort(), &g_err, kSiteEsDs,
-                             p.wait_limit_ns))
-        return;
-      uint8_t* row = sh.ds_ptr(buf) + kr * 128;
+      if constexpr (DQ) {
+        if (!mbar_wait_bounded(sh.ds_free(buf), ((sit >> 1) & 1) ^ 1, sh.abort(), &g_err, kSiteEsDs,
+                               p.wait_limit_ns))
+          return;
+        uint8_t* row = sh.ds_ptr(buf) + kr * 128;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(row + (((4 * H + j) ^ (kr & 7)) << 4)) =
-            make_uint4(dd[4 * j], dd[4 * j + 1], dd[4 * j + 2], dd[4 * j + 3]);
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(row + (((4 * H + j) ^ (kr & 7)) << 4)) =
+              make_uint4(dd[4 * j], dd[4 * j + 1], dd[4 * j + 2], dd[4 * j + 3]);
+      }
       tmem_st_wait();
-      fence_proxy_async_smem();
+      if constexpr (DQ) fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(sh.p_ready(buf));
     }
@@ -768,7 +774,7 @@ __device__ void elementwise_role(const Shared<kD>& sh, const uint32_t tmem, cons
 // two row-major FP32 staging tiles in shared memory (queries 0-31 and 32-63
 // of the block, 32 x 128 each); the reduce issuer adds each into the FP32
 // accumulator.  At the end of a unit it writes dK (scaled) and dV.
-template <int kD, bool PACKED, bool DYN>
+template <int kD, bool PACKED, bool DYN, bool DQ>
 __device__ void dq_role(const Shared<kD>& sh, const uint32_t tmem, const BwdParams& p, const int total_units) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int wq = warp & 3;
@@ -782,7 +788,7 @@ __device__ void dq_role(const Shared<kD>& sh, const uint32_t tmem, const BwdPara
     if (u < 0) break;
     const Unit w = decode_unit<PACKED>(u, p);
     bool stop = false;
-    for (int s = 0; s < w.steps; ++s, ++sit) {
+    for (int s = 0; DQ && s < w.steps; ++s, ++sit) {
       const int buf = sit & 1;
       if (!mbar_wait_bounded(sh.dq_full(buf), (sit >> 1) & 1, sh.abort(), &g_err, kSiteDqFull, p.wait_limit_ns)) {
         stop = true;
@@ -881,8 +887,16 @@ __device__ void dq_role(const Shared<kD>& sh, const uint32_t tmem, const BwdPara
 // only from key block n to block n - 1 of the same head, which has the
 // smaller unit index in every schedule, and no ticket is held across units,
 // so the waits cannot form a cycle.
-template <int kD, bool PACKED, bool DYN>
+template <int kD, bool PACKED, bool DYN, bool DQ>
 __device__ void reduce_role(const Shared<kD>& sh, const CUtensorMap* tdq, const BwdParams& p, const int total_units) {
+  if constexpr (!DQ) {
+    // dQ is computed by its own kernel: only the unit announcements of the
+    // dynamic schedule are acknowledged here
+    if constexpr (DYN)
+      for (int k = 0;; ++k)
+        if (next_unit<kD, DYN>(sh, k, p, kSiteDqFull, total_units) < 0) break;
+    return;
+  }
   uint32_t sit = 0;
   bool pending1 = false;   // tile 1 of the previous step is still being read
   int* held = nullptr;     // deterministic mode: ticket of the previous step, not yet released
@@ -954,7 +968,7 @@ done:
   if (held) release_held();
 }
 
-template <int kD, bool PACKED, bool DYN>
+template <int kD, bool PACKED, bool DYN, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1012,21 +1026,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // register split (sums to the 512 x 128 the block was launched with)
   if (warp < 4) {
     reg_alloc<160>();
-    elementwise_role<kD, PACKED, DYN, 0>(sh, tmem, p, total_units);
+    elementwise_role<kD, PACKED, DYN, DQ, 0>(sh, tmem, p, total_units);
   } else if (warp < 8) {
-    dq_role<kD, PACKED, DYN>(sh, tmem, p, total_units);
+    dq_role<kD, PACKED, DYN, DQ>(sh, tmem, p, total_units);
   } else if (warp < 12) {
     reg_dealloc<64>();
     if (warp == 8) {
       if ((threadIdx.x % 32) == 0) producer_role<kD, PACKED, DYN>(sh, &tm_q, &tm_k, &tm_v, &tm_do, p, total_units);
     } else if (warp == 9) {
-      mma_role<kD, PACKED, DYN>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
+      mma_role<kD, PACKED, DYN, DQ>(sh, tmem, p, total_units);   // converged warp; one elected lane issues
     } else if (warp == 10) {
-      if ((threadIdx.x % 32) == 0) reduce_role<kD, PACKED, DYN>(sh, &tm_dqacc, p, total_units);
+      if ((threadIdx.x % 32) == 0) reduce_role<kD, PACKED, DYN, DQ>(sh, &tm_dqacc, p, total_units);
     }
   } else {
     reg_alloc<160>();
-    elementwise_role<kD, PACKED, DYN, 1>(sh, tmem, p, total_units);
+    elementwise_role<kD, PACKED, DYN, DQ, 1>(sh, tmem, p, total_units);
   }
   if (ld_shared_volatile(sh.abort())) {
     const uint64_t t0 = globaltimer_ns();
@@ -1044,6 +1058,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
+// The main kernel, with (DQ) or without its dQ product.
+template <int kD, bool DQ>
+fa_status launch_main(const BwdLaunch& L, bool packed, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq, cudaStream_t stream) {
+  const BwdParams& p = L.p;
+  fa_status st;
+  if ((st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, false, false, DQ>),
+                           bwd::Layout<kD>::kDynamic)) != FA_OK ||
+      (st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, false, true, DQ>),
+                           bwd::Layout<kD>::kDynamic)) != FA_OK ||
+      (st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, true, true, DQ>),
+                           bwd::Layout<kD>::kDynamic)) != FA_OK)
+    return st;
+  // packed: the number of key blocks is only known on the device; this
+  // bound (every sequence adds at most one partial block) sizes the grid
+  const long long units = packed ? ((long long)p.Sk / bwd::kBN + p.B) * p.Hkv
+                                 : (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
+  const int grid = (int)(units < L.num_sms ? units : L.num_sms);
+  constexpr int kSmem = bwd::Layout<kD>::kDynamic;
+  // packed layouts always use the dynamic schedule (their units differ in
+  // length); dense ones as chosen by the caller (sched_dynamic)
+  if (packed)
+    bwd::bwd_kernel<kD, true, true, DQ><<<grid, bwd::kThreads, kSmem, stream>>>(tq, tk, tv, tdo, tdq, p);
+  else if (p.sched_dynamic)
+    bwd::bwd_kernel<kD, false, true, DQ><<<grid, bwd::kThreads, kSmem, stream>>>(tq, tk, tv, tdo, tdq, p);
+  else
+    bwd::bwd_kernel<kD, false, false, DQ><<<grid, bwd::kThreads, kSmem, stream>>>(tq, tk, tv, tdo, tdq, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 template <int kD>
 fa_status launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   const BwdParams& p = L.p;
@@ -1057,7 +1101,11 @@ fa_status launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
   // accumulator and tickets
   const long long heads_rt = packed ? (long long)p.Hq : (long long)p.B * p.Hq;
   const long long rows = heads_rt * p.sq_pad;
-  const long long n_tickets = p.deterministic ? heads_rt * p.nqb * 2 : 0;
+  // split: dK / dV from the main kernel without its dQ product, dQ from its
+  // own kernel (no accumulator, no tickets, no post pass)
+  const bool split = L.split_dq && !L.pair;
+  float* acc = split ? nullptr : p.dq_acc;
+  const long long n_tickets = (p.deterministic && !split) ? heads_rt * p.nqb * 2 : 0;
   long long pre_blocks = (rows * 32 + 255) / 256;
   if (pre_blocks > 16 * L.num_sms) pre_blocks = 16 * L.num_sms;
   if (pre_blocks < 1) pre_blocks = 1;
@@ -1065,12 +1113,12 @@ fa_status launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
     bwd::plan_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.B, p.Sq, p.Hkv, p.sched_group, p.plan, p.order);
     bwd::pre_packed_kernel<kD><<<(unsigned)pre_blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
-        p.cu_seqlens, p.plan, p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq,
+        p.cu_seqlens, p.plan, p.ndelta, p.nlse2, acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq,
         p.sq_pad);
   } else {
     bwd::pre_kernel<kD><<<(unsigned)pre_blocks, 256, 0, stream>>>(
         reinterpret_cast<const __nv_bfloat16*>(p.o), reinterpret_cast<const __nv_bfloat16*>(p.dout), p.lse,
-        p.ndelta, p.nlse2, p.dq_acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq, p.sq_pad);
+        p.ndelta, p.nlse2, acc, p.tickets, n_tickets, p.sched, p.B, p.Hq, p.Sq, p.sq_pad);
   }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
@@ -1084,29 +1132,11 @@ fa_status launch_bwd_d(const BwdLaunch& L, cudaStream_t stream) {
     if ((st = make_tmap_rows_heads_d(&tdo, p.dout, rows_q, p.Hq, p.D, bwd::kBM)) != FA_OK) return st;
     if ((st = make_tmap_rows_heads_d(&tk, L.k, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
     if ((st = make_tmap_rows_heads_d(&tv, L.v, rows_k, p.Hkv, p.D, bwd::kBN)) != FA_OK) return st;
-    if ((st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, false, false>),
-                             bwd::Layout<kD>::kDynamic)) != FA_OK ||
-        (st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, false, true>),
-                             bwd::Layout<kD>::kDynamic)) != FA_OK ||
-        (st = prepare_kernel(reinterpret_cast<const void*>(bwd::bwd_kernel<kD, true, true>),
-                             bwd::Layout<kD>::kDynamic)) != FA_OK)
-      return st;
-    // packed: the number of key blocks is only known on the device; this
-    // bound (every sequence adds at most one partial block) sizes the grid
-    const long long units = packed ? ((long long)p.Sk / bwd::kBN + p.B) * p.Hkv
-                                   : (long long)((p.Sk + bwd::kBN - 1) / bwd::kBN) * p.B * p.Hkv;
-    const int grid = (int)(units < L.num_sms ? units : L.num_sms);
-    // packed layouts always use the dynamic schedule (their units differ in
-    // length); dense ones as chosen by the caller (sched_dynamic)
-    if (packed)
-      bwd::bwd_kernel<kD, true, true><<<grid, bwd::kThreads, bwd::Layout<kD>::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
-    else if (p.sched_dynamic)
-      bwd::bwd_kernel<kD, false, true><<<grid, bwd::kThreads, bwd::Layout<kD>::kDynamic, stream>>>(tq, tk, tv, tdo, tdq, p);
-    else
-      bwd::bwd_kernel<kD, false, false><<<grid, bwd::kThreads, bwd::Layout<kD>::kDynamic, stream>>>(tq, tk, tv, tdo, tdq,
-                                                                                          p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (split) st = launch_main<kD, false>(L, packed, tq, tk, tv, tdo, tdq, stream);
+    else st = launch_main<kD, true>(L, packed, tq, tk, tv, tdo, tdq, stream);
+    if (st != FA_OK) return st;
   }
+  if (split) return launch_bwd_dq(L, stream);
 
   // post: dQ = BF16(scale * accumulator)
   const long long n8 = (long long)rows_q * p.Hq * p.D / 8;

@@ -49,6 +49,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "q_sched.cuh"
 #include "softmax_math.cuh"
 
 namespace fa {
@@ -59,7 +60,8 @@ __device__ DeviceError g_err;
 constexpr int kThreads = 512;
 constexpr int kBM = 128;      // query rows per tile
 constexpr int kBN = 128;      // keys per block
-constexpr int kPairRows = 2 * kBM;
+constexpr int kPairRows = qs::kPairRows;
+using qs::PackedSched;
 
 // Failure sites recorded with FA_ERR_TIMEOUT.
 enum Site { kSiteSoftmaxS = 1, kSiteCorrP, kSiteCorrO, kSiteMmaQ, kSiteMmaKV, kSiteMmaO, kSiteProdQ, kSiteProdKV };
@@ -78,10 +80,8 @@ struct Layout {
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem slot, abort, warp flags[8]
   static constexpr int kStats = kMisc + 64;            // scale/l/m/lr: 4 x [2][128] floats
   static constexpr int kSched = kStats + 4 * 2 * kBM * 4;
-  // packed schedule: start[S], len[S], seq[S], unit prefix [S+1],
-  // pair-group prefix [P+1], header[4]  (ints)
-  static constexpr int kSchedInts = 3 * kMaxPackedSeqs + (kMaxPackedSeqs + 1) + (kMaxPairsPerSeq + 1) + 4;
-  static constexpr int kSchedBytes = VARLEN ? 4 * kSchedInts : 0;
+  // packed schedule tables (qs::PackedSched)
+  static constexpr int kSchedBytes = VARLEN ? qs::kSchedBytes : 0;
   // the K/V ring last, 1024-byte aligned (whole 128-byte swizzle atoms)
   static constexpr int kKV = (kSched + kSchedBytes + 1023) / 1024 * 1024;
   static constexpr int dynamic_bytes(int stages) { return kKV + stages * kTileBytes + kSmemAlignSlack; }
@@ -89,27 +89,11 @@ struct Layout {
   static_assert(kMaxDynamic <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
-// One work unit: a pair of 128-row query tiles of one (sequence, head).
-struct Unit {
-  int h;          // query head
-  int pair;       // pair index inside the sequence
-  int q_tok0;     // token index (row of the [rows, H, D] view) of the sequence's first query
-  int k_tok0;     // same for keys
-  int seq_q, seq_k;
-  int b;          // batch / sequence index (for LSE addressing)
+// One work unit: a pair of 128-row query tiles of one (sequence, head), and
+// the key blocks each tile visits.
+struct Unit : qs::QUnit {
   int nt[2];      // KV blocks each query tile sees (0: no valid row, or no visible key)
   int n;          // KV blocks to load: max(nt[0], nt[1])
-};
-
-// Packed-length schedule tables (shared memory).  Sequences are sorted by
-// length, longest first (ties by index).
-struct PackedSched {
-  int* start;      // [nseq] first token of the i-th longest sequence
-  int* len;        // [nseq] its length
-  int* seq;        // [nseq] its index
-  int* uprefix;    // [nseq+1] non-causal: units before the i-th longest sequence
-  int* gprefix;    // [P+1]   causal: units before pair group k (pair index P-1-k)
-  int* header;     // [0] total units, [1] max pairs P, [2] total tokens, [3] bad input
 };
 
 // KV blocks the query tile starting at row `row0` needs: 0 when the tile has
@@ -130,135 +114,11 @@ __device__ __forceinline__ int tile_kv_blocks(int row0, int seq_q, int seq_k) {
 template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p, const PackedSched& ps) {
   Unit w;
-  if (!VARLEN) {
-    const int npairs = (p.Sq + kPairRows - 1) / kPairRows;
-    const int BH = p.B * p.Hq;
-    int bh;
-    if (CAUSAL) {
-      // longest first within groups of sched_group (batch, head) pairs: a
-      // group's pairs near the end of the sequence (the most key blocks)
-      // first, every head of the group at each level, group after group.
-      // The groups bound how many heads' K/V are in flight at once, so that
-      // the key blocks a head's pairs share stay in L2.
-      const int G = p.sched_group;
-      const int grp = u / (G * npairs), r = u % (G * npairs);
-      const int gh = min(G, BH - grp * G);   // heads of this (possibly last, smaller) group
-      w.pair = npairs - 1 - r / gh;
-      bh = grp * G + r % gh;
-    } else {       // every pair costs the same: keep a head's pairs together
-      bh = u / npairs;
-      w.pair = u % npairs;
-    }
-    w.b = bh / p.Hq;
-    w.h = bh % p.Hq;
-    w.q_tok0 = w.b * p.Sq;
-    w.k_tok0 = w.b * p.Sk;
-    w.seq_q = p.Sq;
-    w.seq_k = p.Sk;
-  } else {
-    const int nseq = p.B;
-    int i;
-    if (CAUSAL) {
-      // groups of equal pair index, highest first; group k holds pair P-1-k of
-      // every sequence that has it (a prefix of the longest-first order)
-      const int P = ps.header[1];
-      int lo = 0, hi = P - 1;
-      while (lo < hi) {  // last k with gprefix[k] <= u
-        const int mid = (lo + hi + 1) >> 1;
-        if (ps.gprefix[mid] <= u) lo = mid; else hi = mid - 1;
-      }
-      w.pair = P - 1 - lo;
-      const int idx = u - ps.gprefix[lo];
-      i = idx / p.Hq;
-      w.h = idx % p.Hq;
-    } else {
-      int lo = 0, hi = nseq - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (ps.uprefix[mid] <= u) lo = mid; else hi = mid - 1;
-      }
-      i = lo;
-      const int rem = u - ps.uprefix[i];
-      const int np = (ps.len[i] + kPairRows - 1) / kPairRows;
-      w.h = rem / np;
-      w.pair = rem % np;
-    }
-    w.b = ps.seq[i];
-    w.q_tok0 = ps.start[i];
-    w.k_tok0 = ps.start[i];
-    w.seq_q = ps.len[i];
-    w.seq_k = ps.len[i];
-  }
+  static_cast<qs::QUnit&>(w) = qs::decode_pair_unit<CAUSAL, VARLEN>(u, p, ps);
   w.nt[0] = tile_kv_blocks<CAUSAL>(w.pair * kPairRows, w.seq_q, w.seq_k);
   w.nt[1] = tile_kv_blocks<CAUSAL>(w.pair * kPairRows + kBM, w.seq_q, w.seq_k);
   w.n = max(w.nt[0], w.nt[1]);
   return w;
-}
-
-// Builds the packed-length tables cooperatively (all threads) and returns the
-// number of work units.  Invalid offsets are recorded as FA_ERR_INVALID_ARG
-// and leave the CTA with no work.
-template <bool CAUSAL>
-__device__ int build_packed_sched(const FwdParams& p, PackedSched& ps, uint8_t* base) {
-  const int nseq = p.B;
-  ps.start = reinterpret_cast<int*>(base);
-  ps.len = ps.start + kMaxPackedSeqs;
-  ps.seq = ps.len + kMaxPackedSeqs;
-  ps.uprefix = ps.seq + kMaxPackedSeqs;
-  ps.gprefix = ps.uprefix + kMaxPackedSeqs + 1;
-  ps.header = ps.gprefix + kMaxPairsPerSeq + 1;
-  if (threadIdx.x == 0) ps.header[3] = 0;
-  __syncthreads();
-  // validate: cu[0] == 0, non-decreasing, cu[B] == total, lengths <= limit
-  for (int b = threadIdx.x; b < nseq; b += blockDim.x) {
-    const int s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
-    bool bad = s1 < s0 || (s1 - s0) > kMaxPairsPerSeq * kPairRows;
-    if (b == 0) bad |= s0 != 0;
-    if (b == nseq - 1) bad |= s1 != p.Sq;
-    if (bad) ps.header[3] = 1;
-  }
-  __syncthreads();
-  if (ps.header[3]) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicCAS(&g_err.status, 0, FA_ERR_INVALID_ARG);
-    return 0;
-  }
-  // rank of each sequence in longest-first order (ties by index)
-  for (int b = threadIdx.x; b < nseq; b += blockDim.x) {
-    const int Lb = p.cu_seqlens[b + 1] - p.cu_seqlens[b];
-    int rank = 0;
-    for (int c = 0; c < nseq; ++c) {
-      const int Lc = p.cu_seqlens[c + 1] - p.cu_seqlens[c];
-      rank += (Lc > Lb) || (Lc == Lb && c < b);
-    }
-    ps.start[rank] = p.cu_seqlens[b];
-    ps.len[rank] = Lb;
-    ps.seq[rank] = b;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int i = 0; i < nseq; ++i) {
-      ps.uprefix[i] = acc;
-      acc += ((ps.len[i] + kPairRows - 1) / kPairRows) * p.Hq;
-    }
-    ps.uprefix[nseq] = acc;
-    const int P = nseq ? (ps.len[0] + kPairRows - 1) / kPairRows : 0;
-    // causal groups: pair index P-1-k for k = 0..P-1; members are the
-    // sequences with more than that many pairs (a prefix of the order)
-    int g = 0, members = 0;
-    for (int k = 0; k < P; ++k) {
-      const int pi = P - 1 - k;   // descending, so the member prefix only grows
-      while (members < nseq && (ps.len[members] + kPairRows - 1) / kPairRows > pi) ++members;
-      ps.gprefix[k] = g;
-      g += members * p.Hq;
-    }
-    ps.gprefix[P] = g;
-    ps.header[0] = acc;   // both orders enumerate the same units
-    ps.header[1] = P;
-    ps.header[2] = p.Sq;
-  }
-  __syncthreads();
-  return ps.header[0];
 }
 
 // Position in the K/V ring: stage index and the parity of its barriers'
@@ -754,9 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   PackedSched ps{};
   int total_units;
   if (VARLEN) {
-    total_units = build_packed_sched<CAUSAL>(p, ps, smem + L::kSched);
+    total_units = qs::build_packed_sched(p, ps, smem + L::kSched, &g_err);
   } else {
-    total_units = ((p.Sq + kPairRows - 1) / kPairRows) * p.B * p.Hq;
+    total_units = qs::dense_units(p);
   }
   tc_fence_before();
   __syncthreads();

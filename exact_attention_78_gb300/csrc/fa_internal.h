@@ -78,7 +78,8 @@ struct BwdLaunch {
   const void* v;
   BwdParams p;
   int num_sms;
-  bool pair;   // main kernel on CTA pairs (paired MMAs) rather than single CTAs
+  bool pair;       // main kernel on CTA pairs (paired MMAs) rather than single CTAs
+  bool split_dq;   // dK / dV from the main kernel without its dQ product, dQ from its own kernel
 };
 
 // Workspace carve-up of the backward pass (all offsets 256-byte aligned).
@@ -106,6 +107,7 @@ fa_status prepare_kernel(const void* func, int bytes);
 fa_status launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 fa_status launch_bwd(const BwdLaunch& L, cudaStream_t stream);
 fa_status launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream);
+fa_status launch_bwd_dq(const BwdLaunch& L, cudaStream_t stream);
 fa_status launch_diag_exp2(const float* x, float* y_emu, float* y_hw, long long n, cudaStream_t stream);
 fa_status launch_diag_wait(unsigned long long limit_ns, cudaStream_t stream);
 
@@ -114,6 +116,7 @@ fa_status launch_diag_wait(unsigned long long limit_ns, cudaStream_t stream);
 fa_status fwd_take_device_error();
 fa_status bwd_take_device_error();
 fa_status bwd_pair_take_device_error();
+fa_status bwd_dq_take_device_error();
 fa_status diag_take_device_error();
 
 // Shared-memory alignment slack added to every dynamic allocation.

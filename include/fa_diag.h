@@ -99,8 +99,17 @@ FA_API fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o,
  *   scores_first    1: the next step's S^T product is issued before the
  *                   MMA warp waits for the dQ read-out of its TMEM buffer;
  *                   0: after.
+ *   split_dq        1: the backward runs as two main kernels: one per key
+ *                   block accumulating dK and dV (no dQ product), one per
+ *                   128-row query tile accumulating dQ over the key blocks
+ *                   in order inside tensor memory and writing it directly;
+ *                   no FP32 dQ accumulator, no atomics, and the same bits on
+ *                   every run.  0: one main kernel adds dQ partial sums into
+ *                   the FP32 accumulator (in deterministic mode in ticket
+ *                   order).  Default: 1 in deterministic mode, 0 otherwise.
+ *                   The paired kernel ignores it.
  * FA_ERR_INVALID_ARG for a value out of range (paired, schedule,
- * reverse_blocks or scores_first > 1, head_group 0).
+ * reverse_blocks, scores_first or split_dq > 1, head_group 0).
  */
 typedef struct {
   int paired;
@@ -108,6 +117,7 @@ typedef struct {
   int head_group;
   int reverse_blocks;
   int scores_first;
+  int split_dq;
 } fa_bwd_tuning;
 
 /* The defaults fa_bwd() uses: paired 0, every other knob -1 (chosen per

@@ -135,18 +135,18 @@ def test_backward_tuning_validation(lib):
     from exact_attention_78_gb300.binding import BwdTuning
     d = lib.fa_bwd_default_tuning()
     assert d.paired == 0
-    assert (d.schedule, d.head_group, d.reverse_blocks, d.scores_first) == (-1, -1, -1, -1)
+    assert (d.schedule, d.head_group, d.reverse_blocks, d.scores_first, d.split_dq) == (-1, -1, -1, -1, -1)
     # one knob out of range at a time, on top of the defaults (only rejected
     # calls are made: the pointers are not device memory)
     bad_values = {"paired": (2, 7), "schedule": (2,), "head_group": (0,), "reverse_blocks": (2,),
-                  "scores_first": (3,)}
+                  "scores_first": (3,), "split_dq": (2,)}
     for name, vals in bad_values.items():
         for val in vals:
             bad = lib.fa_bwd_default_tuning()
             setattr(bad, name, val)
             assert lib.fa_bwd_ex(A, A, A, A, A, A, A, A, A, 1, 2, 2, 128, 128, 128, 0, 0.125, None, 0, A, 1 << 40,
                                  ctypes.byref(bad), None) == 1, (name, val)
-    assert len(BwdTuning._fields_) == 5
+    assert len(BwdTuning._fields_) == 6
 
 
 def test_binding_rejects_unknown_backward_knob():

@@ -199,3 +199,52 @@ def test_sweep_config_sampled_heads(fa, D, S, causal):
     for t in grads:
         assert bool(torch.isfinite(t.float()).all())
     _heads_vs_oracle(q, k, v, do, grads, causal, w.scale, [(0, 0), (w.B - 1, 15)])
+
+
+def _grads_tuned(fa, q, k, v, do, causal, deterministic, tuning):
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal=causal)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, deterministic=deterministic, tuning=tuning)
+    assert fa.get_device_error() == 0
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk", [
+    (2, 4, 2, 300, 300),     # grouped heads, ragged rows and keys
+    (1, 2, 1, 1000, 1000),   # several 64-key blocks and query tiles
+    (1, 2, 2, 129, 257),     # Sq < Sk
+    (1, 2, 2, 520, 300),     # Sq > Sk: causal leaves the first rows without keys
+    (1, 1, 1, 1, 1),
+])
+def test_split_dq_kernel(fa, D, causal, B, Hq, Hkv, Sq, Sk):
+    """The split backward (dK / dV from the main kernel without its dQ
+    product, dQ from the query-tile kernel): oracle parity, bitwise repeats,
+    and agreement with the fused kernel's atomic dQ."""
+    q, k, v, do = _inputs(B, Hq, Hkv, Sq, Sk, seed=17, D=D)
+    a = _grads_tuned(fa, q, k, v, do, causal, False, {"split_dq": 1})
+    _check(a, q, k, v, do, causal)
+    b = _grads_tuned(fa, q, k, v, do, causal, False, {"split_dq": 1})
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    c = _grads_tuned(fa, q, k, v, do, causal, False, {"split_dq": 0})
+    for x, y in zip(a, c):
+        if np.linalg.norm(f64(y)) > 1e-9:
+            assert rel_fro(f64(x), f64(y)) <= 2e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_deterministic_ticket_path_still_available(fa, causal):
+    """split_dq = 0 keeps the fused kernel's ticket-ordered dQ additions in
+    deterministic mode: bitwise repeatable and equal (to rounding) to the
+    default split path."""
+    q, k, v, do = _inputs(2, 4, 2, 700, 700, seed=18)
+    a = _grads_tuned(fa, q, k, v, do, causal, True, {"split_dq": 0})
+    b = _grads_tuned(fa, q, k, v, do, causal, True, {"split_dq": 0})
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    _check(a, q, k, v, do, causal)
+    c = _gpu_grads(fa, q, k, v, do, causal, deterministic=True)
+    for x, y in zip(a, c):
+        assert rel_fro(f64(x), f64(y)) <= 2e-3
