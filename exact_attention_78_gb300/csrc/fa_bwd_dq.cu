@@ -12,9 +12,10 @@
 //     S  = Q K_j^T,  dP = dO V_j^T            (M = 128 queries, N = 64 keys)
 //     P  = exp2(S * scale * log2 e - LSE2),  dS = P * (dP - Delta)
 //     dQ += dS K_j                            (M = 128, N = D, K = 64 keys)
-// with the score products of block j + 1 issued while the elementwise pass
-// of block j runs (two score buffers in tensor memory), and dQ written as
-// BF16 (times scale) at the end of the tile.  Its companion, the main
+// with the score products of the next blocks issued while the elementwise
+// pass of block j runs (three score buffers in tensor memory, two for packed
+// layouts at D = 128, where shared memory is shorter), and dQ written as BF16
+// (times scale) at the end of the tile.  Its companion, the main
 // backward kernel without its dQ product, accumulates dK and dV.
 //
 // Thread layout (320 threads, one CTA per SM):
@@ -24,14 +25,15 @@
 //   warp  8     TMA producer (one lane)
 //   warp  9     TMEM owner + MMA issuer (converged warp, one elected lane)
 //
-// Tensor memory: score buffers b = 0, 1 with S at 128 b (64 columns) and dP
+// Tensor memory: score buffers b < kSB with S at 128 b (64 columns) and dP
 // at 128 b + 64; dS as BF16 pairs over columns 0-15 and 32-47 of the S
 // region (one half per warpgroup, each inside the columns it has read); dQ
-// in [256, 256 + D).
+// in [128 kSB, 128 kSB + D).
 //
 // Shared memory: Q and dO of the current and the next tile (two buffers),
-// a ring of (K_j, V_j) blocks, barriers, and for packed layouts the
-// longest-first schedule tables.
+// a ring of K_j blocks (held from the score product to the dQ product of a
+// block) and a shorter ring of V_j blocks (read by the dP product only),
+// barriers, and for packed layouts the longest-first schedule tables.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -75,17 +77,23 @@ struct Layout {
   static constexpr int kQChunk = kBM * 128;           // 128 rows x 64 features
   static constexpr int kKTile = kBN * D * 2;          // K_j or V_j: 64 keys x D
   static constexpr int kKChunk = kBN * 128;           // 64 keys x 64 features (8 KB)
-  static constexpr int kStages = (D == 64) ? 4 : (VARLEN ? 2 : 3);
+  static constexpr bool kShort = (D == 128 && VARLEN);   // packed D = 128: less shared memory left
+  static constexpr int kSB = kShort ? 2 : 3;             // score buffers in tensor memory
+  static constexpr int kKSt = kShort ? 2 : 4;            // K ring: blocks j .. j + kSB - 1 held, one loading
+  static constexpr int kVSt = (D == 64) ? 3 : 2;         // V ring
   static constexpr int kQ = 0;                                      // [2 buffers][Q | dO]
-  static constexpr int kKV = kQ + 2 * 2 * kTileBytes;               // [kStages][K | V]
-  static constexpr int kBars = kKV + kStages * 2 * kKTile;
-  // qd_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_ready[2], dq_full, dq_empty
-  static constexpr int kNumBars = 4 + 2 * kStages + 6;
+  static constexpr int kK = kQ + 2 * 2 * kTileBytes;                // [kKSt] K_j
+  static constexpr int kV = kK + kKSt * kKTile;                     // [kVSt] V_j
+  static constexpr int kBars = kV + kVSt * kKTile;
+  // qd_full[2], q_empty[2], k_full[kKSt], k_empty[kKSt], v_full[kVSt], v_empty[kVSt],
+  // s_full[kSB], p_ready[kSB], dq_full, dq_empty
+  static constexpr int kNumBars = 4 + 2 * kKSt + 2 * kVSt + 2 * kSB + 2;
   static constexpr int kMisc = kBars + kNumBars * 8;                // tmem slot, abort flag
   static constexpr int kSched = kMisc + 64;
   static constexpr int kTotal = kSched + (VARLEN ? qs::kSchedBytes : 0);
   static constexpr int kDynamic = kTotal + kSmemAlignSlack;
-  static_assert(kKV % 1024 == 0 && kBars % 1024 == 0, "tile alignment");
+  static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kBars % 1024 == 0, "tile alignment");
+  static_assert(kSB * 128 + D <= 512, "tensor memory");
   static_assert(kDynamic <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
@@ -97,21 +105,24 @@ struct Shared {
   FA_DEV uint32_t bar(int i) const { return sbase + L::kBars + 8 * i; }
   FA_DEV uint32_t qd_full(int q) const { return bar(q); }           // Q and dO of buffer q landed
   FA_DEV uint32_t q_empty(int q) const { return bar(2 + q); }       // their score products are done
-  FA_DEV uint32_t kv_full(int s) const { return bar(4 + s); }
-  FA_DEV uint32_t kv_empty(int s) const { return bar(4 + L::kStages + s); }
-  FA_DEV uint32_t s_full(int b) const { return bar(4 + 2 * L::kStages + b); }
-  FA_DEV uint32_t p_ready(int b) const { return bar(6 + 2 * L::kStages + b); }   // dS of buffer b in TMEM
-  FA_DEV uint32_t dq_full() const { return bar(8 + 2 * L::kStages); }
-  FA_DEV uint32_t dq_empty() const { return bar(9 + 2 * L::kStages); }
+  FA_DEV uint32_t k_full(int s) const { return bar(4 + s); }
+  FA_DEV uint32_t k_empty(int s) const { return bar(4 + L::kKSt + s); }
+  FA_DEV uint32_t v_full(int s) const { return bar(4 + 2 * L::kKSt + s); }
+  FA_DEV uint32_t v_empty(int s) const { return bar(4 + 2 * L::kKSt + L::kVSt + s); }
+  static constexpr int kB2 = 4 + 2 * L::kKSt + 2 * L::kVSt;
+  FA_DEV uint32_t s_full(int b) const { return bar(kB2 + b); }
+  FA_DEV uint32_t p_ready(int b) const { return bar(kB2 + L::kSB + b); }   // dS of buffer b in TMEM
+  FA_DEV uint32_t dq_full() const { return bar(kB2 + 2 * L::kSB); }
+  FA_DEV uint32_t dq_empty() const { return bar(kB2 + 2 * L::kSB + 1); }
   FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
   FA_DEV uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + L::kMisc); }
   FA_DEV uint32_t q_tile(int q) const { return sbase + L::kQ + q * 2 * L::kTileBytes; }
   FA_DEV uint32_t do_tile(int q) const { return q_tile(q) + L::kTileBytes; }
-  FA_DEV uint32_t k_tile(int s) const { return sbase + L::kKV + s * 2 * L::kKTile; }
-  FA_DEV uint32_t v_tile(int s) const { return k_tile(s) + L::kKTile; }
+  FA_DEV uint32_t k_tile(int s) const { return sbase + L::kK + s * L::kKTile; }
+  FA_DEV uint32_t v_tile(int s) const { return sbase + L::kV + s * L::kKTile; }
 };
 
-constexpr uint32_t kColBuf = 128, kColDPoff = 64, kColDQ = 256;
+constexpr uint32_t kColBuf = 128, kColDPoff = 64;
 
 // One query tile of a unit (a unit is a pair of tiles, see q_sched.cuh).
 struct Tile {
@@ -185,7 +196,7 @@ __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq
                               const qs::PackedSched& ps, int total_units) {
   using L = Layout<D, VARLEN>;
   uint32_t tit = 0;
-  RingPos kv{0, 0u};
+  RingPos kr{0, 0u}, vr{0, 0u};
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const qs::QUnit w = qs::decode_pair_unit<CAUSAL, VARLEN>(u, p, ps);
     const int hk = w.h / p.group;
@@ -203,18 +214,23 @@ __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq
       }
       ++tit;
       for (int j = 0; j < x.nblk; ++j) {
-        if (!mbar_wait_bounded(sh.kv_empty(kv.stage), kv.phase ^ 1u, sh.abort(), &g_err, kSiteProdKV,
+        const int krow = w.k_tok0 + j * kBN;
+        if (!mbar_wait_bounded(sh.k_empty(kr.stage), kr.phase ^ 1u, sh.abort(), &g_err, kSiteProdKV,
                                p.wait_limit_ns))
           return;
-        mbar_arrive_expect_tx(sh.kv_full(kv.stage), 2 * L::kKTile);
+        mbar_arrive_expect_tx(sh.k_full(kr.stage), L::kKTile);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sh.k_tile(kv.stage) + c * L::kKChunk, tk, sh.kv_full(kv.stage), c * 64, hk,
-                      w.k_tok0 + j * kBN);
-          tma_load_3d(sh.v_tile(kv.stage) + c * L::kKChunk, tv, sh.kv_full(kv.stage), c * 64, hk,
-                      w.k_tok0 + j * kBN);
-        }
-        kv = ring_next<L::kStages>(kv);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sh.k_tile(kr.stage) + c * L::kKChunk, tk, sh.k_full(kr.stage), c * 64, hk, krow);
+        kr = ring_next<L::kKSt>(kr);
+        if (!mbar_wait_bounded(sh.v_empty(vr.stage), vr.phase ^ 1u, sh.abort(), &g_err, kSiteProdKV,
+                               p.wait_limit_ns))
+          return;
+        mbar_arrive_expect_tx(sh.v_full(vr.stage), L::kKTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sh.v_tile(vr.stage) + c * L::kKChunk, tv, sh.v_full(vr.stage), c * 64, hk, krow);
+        vr = ring_next<L::kVSt>(vr);
       }
     }
   }
@@ -225,25 +241,34 @@ template <int D, bool CAUSAL, bool VARLEN>
 __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const DqParams& p,
                          const qs::PackedSched& ps, int total_units) {
   using L = Layout<D, VARLEN>;
+  constexpr int kSB = L::kSB;
+  constexpr uint32_t kColDQ = kColBuf * kSB;
   constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);   // S, dP: 128 queries x 64 keys
   constexpr uint32_t kIdQ = idesc_bf16_f32(kBM, D, false, true);      // dQ: A in TMEM, B MN-major
   uint32_t tit = 0, sit = 0;
-  RingPos kv{0, 0u};
+  RingPos kr{0, 0u}, vr{0, 0u};
+  // every step takes the next K block of the ring, so step t's block sits
+  // in K stage t mod kKSt
   auto wait = [&](uint32_t bar, uint32_t parity, int site) -> bool {
     if (!mbar_wait_bounded(bar, parity, sh.abort(), &g_err, site, p.wait_limit_ns)) return false;
     tc_fence_after();
     return true;
   };
-  // S and dP of step t (block at ring position r) into buffer t & 1
-  auto scores = [&](uint32_t t, RingPos r, int qb) -> bool {
-    if (!wait(sh.kv_full(r.stage), r.phase, kSiteMmaKV)) return false;
-    const int buf = t & 1;
+  // S and dP of global step t (the next K and V blocks of the rings) into
+  // buffer t mod kSB; V_j is released as soon as its one product is issued
+  auto scores = [&](uint32_t t, int qb) -> bool {
+    if (!wait(sh.k_full(kr.stage), kr.phase, kSiteMmaKV)) return false;
+    const int buf = t % kSB;
     const uint64_t da = sdesc_sw128(sh.q_tile(qb), 16, 1024);
-    const uint64_t dk = sdesc_sw128(sh.k_tile(r.stage), 16, 1024);
+    const uint64_t dk = sdesc_sw128(sh.k_tile(kr.stage), 16, 1024);
     score_steps<D, 0>(tmem + kColBuf * buf, desc_lo(da), desc_hi(da), desc_lo(dk), desc_hi(dk), kIdS);
+    kr = ring_next<L::kKSt>(kr);
+    if (!wait(sh.v_full(vr.stage), vr.phase, kSiteMmaKV)) return false;
     const uint64_t dg = sdesc_sw128(sh.do_tile(qb), 16, 1024);
-    const uint64_t dv = sdesc_sw128(sh.v_tile(r.stage), 16, 1024);
+    const uint64_t dv = sdesc_sw128(sh.v_tile(vr.stage), 16, 1024);
     score_steps<D, 0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dg), desc_hi(dg), desc_lo(dv), desc_hi(dv), kIdS);
+    mma_commit_w(sh.v_empty(vr.stage));
+    vr = ring_next<L::kVSt>(vr);
     mma_commit_w(sh.s_full(buf));
     return true;
   };
@@ -254,28 +279,28 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
       if (x.nblk == 0) continue;
       const int qb = tit & 1;
       if (!wait(sh.qd_full(qb), (tit >> 1) & 1, kSiteMmaQ)) return;
-      RingPos cur = kv;
-      kv = ring_next<L::kStages>(kv);
-      if (!scores(sit, cur, qb)) return;
+      // prologue: scores of the first kSB - 1 blocks
+      const int pro = min(kSB - 1, x.nblk);
+      for (int j = 0; j < pro; ++j)
+        if (!scores(sit + j, qb)) return;
+      if (pro == x.nblk) mma_commit_w(sh.q_empty(qb));   // every score product of the tile issued
       for (int j = 0; j < x.nblk; ++j, ++sit) {
-        const int buf = sit & 1;
-        RingPos nxt = kv;
-        if (j + 1 < x.nblk) {
-          kv = ring_next<L::kStages>(kv);
-          if (!scores(sit + 1, nxt, qb)) return;
-          if (j + 2 == x.nblk) mma_commit_w(sh.q_empty(qb));   // last score products of the tile issued
-        } else if (j == 0) {
-          mma_commit_w(sh.q_empty(qb));
+        const int buf = sit % kSB;
+        // scores kSB - 1 blocks ahead, into the buffer the previous step's
+        // dQ product has just read (products run in issue order)
+        if (j + kSB - 1 < x.nblk) {
+          if (!scores(sit + kSB - 1, qb)) return;
+          if (j + kSB == x.nblk) mma_commit_w(sh.q_empty(qb));
         }
-        if (!wait(sh.p_ready(buf), (sit >> 1) & 1, kSiteMmaP)) return;
+        if (!wait(sh.p_ready(buf), (sit / kSB) & 1, kSiteMmaP)) return;
         // the previous tile's dQ has been read out before this tile's first
         // (overwriting) dQ product; its score products have run meanwhile
         if (j == 0 && tit > 0 && !wait(sh.dq_empty(), (tit - 1) & 1, kSiteMmaDq)) return;
         // dQ += dS K_j (K_j MN-major: D contiguous, 64-wide chunks 8 KB apart)
-        const uint64_t dk = sdesc_sw128(sh.k_tile(cur.stage), L::kKChunk, 1024);
+        const int kstage = sit % L::kKSt;
+        const uint64_t dk = sdesc_sw128(sh.k_tile(kstage), L::kKChunk, 1024);
         dq_steps<0>(tmem + kColDQ, tmem + kColBuf * buf, desc_lo(dk), desc_hi(dk), kIdQ, j > 0 ? 1u : 0u);
-        mma_commit_w(sh.kv_empty(cur.stage));
-        cur = nxt;
+        mma_commit_w(sh.k_empty(kstage));
       }
       mma_commit_w(sh.dq_full());
       ++tit;
@@ -296,6 +321,8 @@ __device__ void elementwise_role(const Shared<D, VARLEN>& sh, const uint32_t tme
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = pk2(sl2, sl2);
   __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(p.dq);
+  constexpr int kSB = Layout<D, VARLEN>::kSB;
+  constexpr uint32_t kColDQ = kColBuf * kSB;
   uint32_t tit = 0, sit = 0;
   for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
     const qs::QUnit w = qs::decode_pair_unit<CAUSAL, VARLEN>(u, p, ps);
@@ -316,8 +343,8 @@ __device__ void elementwise_role(const Shared<D, VARLEN>& sh, const uint32_t tme
         }
         const uint64_t nl2 = pk2(nl, nl), nd2 = pk2(nd, nd);
         for (int j = 0; j < x.nblk; ++j, ++sit) {
-          const int buf = sit & 1;
-          if (!mbar_wait_bounded(sh.s_full(buf), (sit >> 1) & 1, sh.abort(), &g_err, kSiteEs, p.wait_limit_ns))
+          const int buf = sit % kSB;
+          if (!mbar_wait_bounded(sh.s_full(buf), (sit / kSB) & 1, sh.abort(), &g_err, kSiteEs, p.wait_limit_ns))
             return;
           tc_fence_after();
           const uint32_t tb = tl + kColBuf * buf;
@@ -408,11 +435,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sh.qd_full(q), 1);
       mbar_init(sh.q_empty(q), 1);
     }
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(sh.kv_full(s), 1);
-      mbar_init(sh.kv_empty(s), 1);
+    for (int s = 0; s < L::kKSt; ++s) {
+      mbar_init(sh.k_full(s), 1);
+      mbar_init(sh.k_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int s = 0; s < L::kVSt; ++s) {
+      mbar_init(sh.v_full(s), 1);
+      mbar_init(sh.v_empty(s), 1);
+    }
+    for (int b = 0; b < L::kSB; ++b) {
       mbar_init(sh.s_full(b), 1);
       mbar_init(sh.p_ready(b), 256);
     }
