@@ -118,6 +118,27 @@ def test_packed_deterministic_is_bitwise_repeatable(fa, causal):
         assert rel_fro(f64(x), f64(y)) <= 2e-3
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_split_dq_kernel(fa, D, causal):
+    """The split backward on packed sequences (dK / dV from the main kernel
+    without its dQ product, dQ from the query-tile kernel over each
+    sequence's own keys), including empty, one-token and tile-boundary
+    lengths: oracle parity and bitwise repeats."""
+    q, k, v, do, cu = _packed([1, 130, 0, 513, 256, 77, 128, 129], 4, 2, seed=21, D=D)
+    qd, kd, vd, dod, cud = (t.cuda() for t in (q, k, v, do, cu))
+    o, lse = fa.fwd(qd, kd, vd, causal=causal, cu_seqlens=cud)
+    runs = []
+    for _ in range(2):
+        g = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, cu_seqlens=cud, deterministic=True,
+                   tuning={"split_dq": 1})
+        assert fa.get_device_error() == 0
+        runs.append(tuple(t.cpu() for t in g))
+    for x, y in zip(*runs):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    _check_full(runs[0], q, k, v, do, cu, causal)
+
+
 def test_packed_matches_dense_for_equal_lengths(fa):
     """Equal-length sequences packed back to back give the dense result."""
     B, S, H = 3, 384, 2
