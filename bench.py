@@ -148,28 +148,41 @@ def code_only(src):
 def measured_traffic(kernel, w):
     """DRAM bytes per launch of `kernel` from the committed ncu record, if it
     was taken on this workload and the kernel sources are unchanged since."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel)
-    if not rec:
+        recs = json.load(f).get(kernel)
+    if not recs or w.packed:
         return None
+    if isinstance(recs, dict):
+        recs = [recs]
+    sha = source_sha(kernel)
+    want = "dense B=%d Hq=Hkv=%d S=%d D=%d %s" % (w.B, w.Hq, w.Sq, w.D, "causal" if w.causal else "non-causal")
+    for rec in recs:
+        if rec["source_sha"] == sha and rec["workload"] == want:
+            return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    return None
+
+
+# The sources each kernel is compiled from (a traffic record holds only while
+# they are unchanged, comments and whitespace aside).
+KERNEL_SOURCES = {
+    "bwd_kernel": ["fa_bwd.cu", "ptx.cuh", "softmax_math.cuh", "exp2_poly.h", "fa_internal.h"],
+    "bwd_pair_kernel": ["fa_bwd_pair.cu", "ptx.cuh", "softmax_math.cuh", "exp2_poly.h", "fa_internal.h"],
+    "fwd_kernel": ["fa_fwd.cu", "q_sched.cuh", "ptx.cuh", "softmax_math.cuh", "exp2_poly.h", "fa_internal.h"],
+    "dq_kernel": ["fa_bwd_dq.cu", "q_sched.cuh", "ptx.cuh", "softmax_math.cuh", "exp2_poly.h", "fa_internal.h"],
+}
+
+
+def source_sha(kernel):
+    import hashlib
     csrc = os.path.join(ROOT, "exact_attention_78_gb300", "csrc")
-    files = {"bwd_kernel": ["fa_bwd.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"],
-             "bwd_pair_kernel": ["fa_bwd_pair.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"],
-             "fwd_kernel": ["fa_fwd.cu", "ptx.cuh", "softmax_math.cuh", "fa_internal.h"]}[kernel]
     m = hashlib.sha256()
-    for fn in files:
+    for fn in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, fn)) as f:
             m.update(code_only(f.read()).encode())
-    if w.packed:
-        return None
-    want = "dense B=%d Hq=Hkv=%d S=%d D=%d %s" % (w.B, w.Hq, w.Sq, w.D, "causal" if w.causal else "non-causal")
-    if m.hexdigest()[:16] != rec["source_sha"] or rec["workload"] != want:
-        return None
-    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    return m.hexdigest()[:16]
 
 
 def workload(args):

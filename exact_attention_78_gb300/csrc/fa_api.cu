@@ -243,6 +243,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
       if (g < 1) g = 1;
       L.p.sched_group = (int)g;
     }
+    L.p.snake = (causal && cu_seqlens == nullptr && Sq >= 4096) ? 1 : 0;
     L.p.wait_limit_ns = kDefaultWaitLimitNs;
     L.D = D;
     L.causal = causal != 0;

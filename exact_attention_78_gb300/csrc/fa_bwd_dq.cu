@@ -66,6 +66,7 @@ struct DqParams {
   int group;               // Hq / Hkv
   int sched_group;         // dense causal: heads per longest-first group
   int sq_pad;              // row-term floats per (batch, head) (dense) / per head (packed)
+  int snake;               // deal the units boustrophedon-wise (q_sched.cuh)
   float scale;
   float scale_log2;
   unsigned long long wait_limit_ns;
@@ -197,7 +198,7 @@ __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq
   using L = Layout<D, VARLEN>;
   uint32_t tit = 0;
   RingPos kr{0, 0u}, vr{0, 0u};
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const qs::QUnit w = qs::decode_pair_unit<CAUSAL, VARLEN>(u, p, ps);
     const int hk = w.h / p.group;
     for (int t = 0; t < 2; ++t) {
@@ -272,7 +273,7 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
     mma_commit_w(sh.s_full(buf));
     return true;
   };
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const qs::QUnit w = qs::decode_pair_unit<CAUSAL, VARLEN>(u, p, ps);
     for (int t = 0; t < 2; ++t) {
       const Tile x = tile_of<CAUSAL>(w, t);
@@ -324,7 +325,7 @@ __device__ void elementwise_role(const Shared<D, VARLEN>& sh, const uint32_t tme
   constexpr int kSB = Layout<D, VARLEN>::kSB;
   constexpr uint32_t kColDQ = kColBuf * kSB;
   uint32_t tit = 0, sit = 0;
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const qs::QUnit w = qs::decode_pair_unit<CAUSAL, VARLEN>(u, p, ps);
     const int diag = w.seq_k - w.seq_q;
     for (int t = 0; t < 2; ++t) {
@@ -540,6 +541,7 @@ fa_status launch_bwd_dq(const BwdLaunch& L, cudaStream_t stream) {
   p.Sk = b.Sk;
   p.group = b.group;
   p.sched_group = b.B * b.Hq;   // dense causal: all heads in one longest-first group
+  p.snake = (b.causal && b.cu_seqlens == nullptr && b.Sq >= 4096) ? 1 : 0;
   p.sq_pad = b.sq_pad;
   p.scale = b.scale;
   p.scale_log2 = b.scale_log2;

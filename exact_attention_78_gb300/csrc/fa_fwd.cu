@@ -171,7 +171,7 @@ __device__ void softmax_role(const int t, const Shared<D, VARLEN>& sh, const uin
   const uint32_t tm_s = tmem + (uint32_t(wq * 32) << 16) + uint32_t(t * kBN);
   const float sl2 = p.scale_log2;
   uint32_t sit = 0;
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
     const int nt = t ? w.nt[1] : w.nt[0];   // (no dynamic index into the struct's array)
     if (nt == 0) continue;
@@ -295,7 +295,7 @@ __device__ void correction_role(const Shared<D, VARLEN>& sh, const uint32_t tmem
   __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(p.o);
   // phase counters per tile: a tile takes part only in the blocks it sees
   uint32_t sit[2] = {0u, 0u}, uit[2] = {0u, 0u};
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
     float fin_l[2] = {0.0f, 0.0f}, fin_lr[2] = {0.0f, 0.0f}, fin_m[2] = {-INFINITY, -INFINITY};
     for (int j = 0; j < w.n; ++j) {
@@ -468,7 +468,7 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
     return true;
   };
 
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
     if (w.n == 0) continue;
     const int n0 = w.nt[0], n1 = w.nt[1];
@@ -543,7 +543,7 @@ __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq
   using L = Layout<D, VARLEN>;
   uint32_t uit = 0;
   RingPos kv{0, 0u};   // next K/V tile to fill
-  for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+  for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const Unit w = decode_unit<CAUSAL, VARLEN>(u, p, ps);
     if (w.n == 0) continue;
     const int hk = w.h / p.group;

@@ -27,6 +27,7 @@ struct FwdParams {
   int stages;              // K/V ring depth (2 .. the kernel's maximum)
   int split_p;             // 1: each half of P (64 keys) is signalled to the MMA warp on its own
   int sched_group;         // dense causal: (batch, head) pairs per group of the longest-first unit order
+  int snake;               // deal the units over the grid boustrophedon-wise (q_sched.cuh)
   unsigned long long wait_limit_ns;
 };
 

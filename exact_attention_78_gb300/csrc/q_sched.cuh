@@ -44,6 +44,22 @@ struct PackedSched {
 constexpr int kSchedInts = 3 * kMaxPackedSeqs + (kMaxPackedSeqs + 1) + (kMaxPairsPerSeq + 1) + 4;
 constexpr int kSchedBytes = 4 * kSchedInts;
 
+// Units of this CTA: the unit order (longest first) is dealt over the
+// persistent grid in rows of G = gridDim.x units, left to right on even rows
+// and right to left on odd ones, so a CTA that takes one of the longest units
+// of a row takes one of the shortest of the next.  CTA c's units are c,
+// 2G - 1 - c, 2G + c, 4G - 1 - c, ...: steps that alternate between
+// 2 (G - 1 - c) + 1 and 2 c + 1 (first_unit / next_unit_step below).
+// Dealing every row left to right instead leaves CTA 0 with the longest unit
+// of every row: on the causal dense workloads that is 4-14% above the mean
+// load (training shape B = 2, S = 8192: 14%), against 0-2% for this order
+// (computed over the sweep's unit costs).  Measured on GB300 (forward,
+// same box): causal B=4 S=4096 +4%, training shape B=2 S=8192 +6%, S=32768
+// +6%, but S=1024 (B=32) -3.5%; so the host asks for it (`snake`) for dense
+// causal calls with S >= 4096 only, and otherwise every step is G.
+FA_DEV int first_step(bool snake) { return snake ? 2 * (int)(gridDim.x - 1 - blockIdx.x) + 1 : (int)gridDim.x; }
+FA_DEV int next_step(int d, bool snake) { return snake ? 2 * (int)gridDim.x - d : d; }
+
 // Dense layout: number of units of the call.
 template <class Prm>
 FA_DEV int dense_units(const Prm& p) {
