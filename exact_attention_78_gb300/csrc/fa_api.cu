@@ -376,15 +376,15 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
     // (the plan kernel writes the order; varlen GQA workload, 64 sequences:
     // groups of 8 / 16 / 32 / 64 / 512 pairs: 1013 / 1006 / 988 / 740 / 661
     // TFLOPS, deterministic 591 / - / 717 / 632 / 569).
-    // The split backward (the deterministic default for the dense layout)
-    // has no ordered additions, so its main kernel takes the schedule of the
-    // atomic mode.  Measured on GB300, deterministic mode, split against the
-    // ticket-ordered fused kernel: dense B=4 H=16 S=4096 D=128 871 vs 717
-    // TFLOPS, causal 732 vs 657, training shape (B=2 S=8192 causal) 808 vs
-    // 716; packed varlen GQA (64 sequences, 128..8192 tokens) 605 vs 728, so
-    // packed layouts keep the ticket path by default.
+    // The split backward (the deterministic default) has no ordered
+    // additions, so its main kernel takes the schedule of the atomic mode.
+    // Measured on GB300, deterministic mode, split (dQ kernel with Q and dO
+    // held in tensor memory) against the ticket-ordered fused kernel: dense
+    // B=4 H=16 S=4096 D=128 927 vs 717 TFLOPS, causal 798 vs 657, training
+    // shape (B=2 S=8192 causal) 888 vs 716, packed varlen GQA (64 sequences,
+    // 128..8192 tokens) 852 vs 728.
     const bool split = tune.paired != 1 &&
-                       (tune.split_dq >= 0 ? tune.split_dq == 1 : (deterministic == 1 && !packed));
+                       (tune.split_dq >= 0 ? tune.split_dq == 1 : deterministic == 1);
     const bool tickets = deterministic && !split;
     {
       const long long bh = (long long)B * Hkv;

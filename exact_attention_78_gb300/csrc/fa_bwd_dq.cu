@@ -13,10 +13,14 @@
 //     P  = exp2(S * scale * log2 e - LSE2),  dS = P * (dP - Delta)
 //     dQ += dS K_j                            (M = 128, N = D, K = 64 keys)
 // with the score products of the next blocks issued while the elementwise
-// pass of block j runs (three score buffers in tensor memory, two for packed
-// layouts at D = 128, where shared memory is shorter), and dQ written as BF16
-// (times scale) at the end of the tile.  Its companion, the main
-// backward kernel without its dQ product, accumulates dK and dV.
+// pass of block j runs (two score buffers in tensor memory at D = 128, three
+// at D = 64), and dQ written as BF16 (times scale) at the end of the tile.
+// Q and dO, the A operands of every score product of the tile, are copied
+// once per tile from shared into tensor memory (tcgen05.cp), so the score
+// products read only K_j and V_j from shared memory: per block of 64 keys
+// that is 384 operand wavefronts of 128 bytes instead of 896, under the
+// shared-memory bandwidth that bounds this kernel otherwise.  Its companion,
+// the main backward kernel without its dQ product, accumulates dK and dV.
 //
 // Thread layout (320 threads, one CTA per SM):
 //   warps 0-3   elementwise for key columns 0-31 of each block, and the dQ
@@ -28,12 +32,14 @@
 // Tensor memory: score buffers b < kSB with S at 128 b (64 columns) and dP
 // at 128 b + 64; dS as BF16 pairs over columns 0-15 and 32-47 of the S
 // region (one half per warpgroup, each inside the columns it has read); dQ
-// in [128 kSB, 128 kSB + D).
+// in [128 kSB, 128 kSB + D); Q and dO of the tile as BF16 pairs (row per
+// lane) in the D columns after it.
 //
-// Shared memory: Q and dO of the current and the next tile (two buffers),
-// a ring of K_j blocks (held from the score product to the dQ product of a
-// block) and a shorter ring of V_j blocks (read by the dP product only),
-// barriers, and for packed layouts the longest-first schedule tables.
+// Shared memory: Q and dO of the next tile (TMA lands them while the current
+// tile runs from its tensor-memory copy), a ring of K_j blocks (held from the
+// score product to the dQ product of a block) and a ring of V_j blocks (read
+// by the dP product only), barriers, and for packed layouts the
+// longest-first schedule tables.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -78,23 +84,26 @@ struct Layout {
   static constexpr int kQChunk = kBM * 128;           // 128 rows x 64 features
   static constexpr int kKTile = kBN * D * 2;          // K_j or V_j: 64 keys x D
   static constexpr int kKChunk = kBN * 128;           // 64 keys x 64 features (8 KB)
-  static constexpr bool kShort = (D == 128 && VARLEN);   // packed D = 128: less shared memory left
-  static constexpr int kSB = kShort ? 2 : 3;             // score buffers in tensor memory
-  static constexpr int kKSt = kShort ? 2 : 4;            // K ring: blocks j .. j + kSB - 1 held, one loading
-  static constexpr int kVSt = (D == 64) ? 3 : 2;         // V ring
-  static constexpr int kQ = 0;                                      // [2 buffers][Q | dO]
-  static constexpr int kK = kQ + 2 * 2 * kTileBytes;                // [kKSt] K_j
+  static constexpr int kSB = (D == 128) ? 2 : 3;         // score buffers in tensor memory
+  static constexpr int kKSt = (D == 128) ? 4 : 6;        // K ring: blocks j .. j + kSB - 1 held, the rest loading
+  static constexpr int kVSt = (D == 128) ? 3 : 4;        // V ring
+  static constexpr int kQ = 0;                                      // [Q | dO] of the next tile
+  static constexpr int kK = kQ + 2 * kTileBytes;                    // [kKSt] K_j
   static constexpr int kV = kK + kKSt * kKTile;                     // [kVSt] V_j
   static constexpr int kBars = kV + kVSt * kKTile;
-  // qd_full[2], q_empty[2], k_full[kKSt], k_empty[kKSt], v_full[kVSt], v_empty[kVSt],
+  // tensor-memory columns of dQ, Q and dO
+  static constexpr uint32_t kColDQ = 128 * kSB;
+  static constexpr uint32_t kColQ = kColDQ + D;
+  static constexpr uint32_t kColDO = kColQ + D / 2;
+  // qd_full, qd_free, qd_tfree, k_full[kKSt], k_empty[kKSt], v_full[kVSt], v_empty[kVSt],
   // s_full[kSB], p_ready[kSB], dq_full, dq_empty
-  static constexpr int kNumBars = 4 + 2 * kKSt + 2 * kVSt + 2 * kSB + 2;
+  static constexpr int kNumBars = 3 + 2 * kKSt + 2 * kVSt + 2 * kSB + 2;
   static constexpr int kMisc = kBars + kNumBars * 8;                // tmem slot, abort flag
   static constexpr int kSched = kMisc + 64;
   static constexpr int kTotal = kSched + (VARLEN ? qs::kSchedBytes : 0);
   static constexpr int kDynamic = kTotal + kSmemAlignSlack;
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kBars % 1024 == 0, "tile alignment");
-  static_assert(kSB * 128 + D <= 512, "tensor memory");
+  static_assert(kColDO + D / 2 <= 512, "tensor memory");
   static_assert(kDynamic <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
@@ -104,26 +113,27 @@ struct Shared {
   uint8_t* base;
   uint32_t sbase;
   FA_DEV uint32_t bar(int i) const { return sbase + L::kBars + 8 * i; }
-  FA_DEV uint32_t qd_full(int q) const { return bar(q); }           // Q and dO of buffer q landed
-  FA_DEV uint32_t q_empty(int q) const { return bar(2 + q); }       // their score products are done
-  FA_DEV uint32_t k_full(int s) const { return bar(4 + s); }
-  FA_DEV uint32_t k_empty(int s) const { return bar(4 + L::kKSt + s); }
-  FA_DEV uint32_t v_full(int s) const { return bar(4 + 2 * L::kKSt + s); }
-  FA_DEV uint32_t v_empty(int s) const { return bar(4 + 2 * L::kKSt + L::kVSt + s); }
-  static constexpr int kB2 = 4 + 2 * L::kKSt + 2 * L::kVSt;
+  FA_DEV uint32_t qd_full() const { return bar(0); }    // Q and dO of the next tile landed in shared memory
+  FA_DEV uint32_t qd_free() const { return bar(1); }    // copied on into tensor memory: the buffer is free
+  FA_DEV uint32_t qd_tfree() const { return bar(2); }   // the tile's last score products done: its copy is free
+  FA_DEV uint32_t k_full(int s) const { return bar(3 + s); }
+  FA_DEV uint32_t k_empty(int s) const { return bar(3 + L::kKSt + s); }
+  FA_DEV uint32_t v_full(int s) const { return bar(3 + 2 * L::kKSt + s); }
+  FA_DEV uint32_t v_empty(int s) const { return bar(3 + 2 * L::kKSt + L::kVSt + s); }
+  static constexpr int kB2 = 3 + 2 * L::kKSt + 2 * L::kVSt;
   FA_DEV uint32_t s_full(int b) const { return bar(kB2 + b); }
   FA_DEV uint32_t p_ready(int b) const { return bar(kB2 + L::kSB + b); }   // dS of buffer b in TMEM
   FA_DEV uint32_t dq_full() const { return bar(kB2 + 2 * L::kSB); }
   FA_DEV uint32_t dq_empty() const { return bar(kB2 + 2 * L::kSB + 1); }
   FA_DEV uint32_t abort() const { return sbase + L::kMisc + 4; }
   FA_DEV uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + L::kMisc); }
-  FA_DEV uint32_t q_tile(int q) const { return sbase + L::kQ + q * 2 * L::kTileBytes; }
-  FA_DEV uint32_t do_tile(int q) const { return q_tile(q) + L::kTileBytes; }
+  FA_DEV uint32_t q_tile() const { return sbase + L::kQ; }
+  FA_DEV uint32_t do_tile() const { return sbase + L::kQ + L::kTileBytes; }
   FA_DEV uint32_t k_tile(int s) const { return sbase + L::kK + s * L::kKTile; }
   FA_DEV uint32_t v_tile(int s) const { return sbase + L::kV + s * L::kKTile; }
 };
 
-constexpr uint32_t kColBuf = 128, kColDPoff = 64;
+constexpr uint32_t kColBuf = 128, kColDPoff = 64;   // score buffer stride; dP within a buffer
 
 // One query tile of a unit (a unit is a pair of tiles, see q_sched.cuh).
 struct Tile {
@@ -155,15 +165,44 @@ FA_DEV size_t row_term(const qs::QUnit& w, int row, const DqParams& p) {
 }
 
 // Unrolled K steps (K = D in 16-wide steps) of S = Q K_j^T or dP = dO V_j^T:
-// both operands K-major, step kk reads 64-wide chunk kk / 4 at byte
-// 32 (kk % 4); A chunks are 128 rows (16 KB) apart, B chunks 64 rows (8 KB).
+// A (Q or dO) in tensor memory, 8 columns per step; B (K_j or V_j) K-major
+// in shared memory, step kk reading 64-wide chunk kk / 4 (chunks 64 rows =
+// 8 KB apart) at byte 32 (kk % 4).
 template <int D, int KK>
-FA_DEV void score_steps(uint32_t d, uint32_t alo, uint32_t ahi, uint32_t blo, uint32_t bhi, uint32_t idesc) {
+FA_DEV void score_steps(uint32_t d, uint32_t a, uint32_t blo, uint32_t bhi, uint32_t idesc) {
   if constexpr (KK < D / 16) {
-    constexpr uint32_t oa = ((KK >> 2) * (kBM * 128) + (KK & 3) * 32) >> 4;
     constexpr uint32_t ob = ((KK >> 2) * (kBN * 128) + (KK & 3) * 32) >> 4;
-    mma_ss_w<oa, ob>(d, alo, ahi, blo, bhi, idesc, KK > 0 ? 1u : 0u);
-    score_steps<D, KK + 1>(d, alo, ahi, blo, bhi, idesc);
+    mma_ts_w<KK * 8, ob>(d, a, blo, bhi, idesc, KK > 0 ? 1u : 0u);
+    score_steps<D, KK + 1>(d, a, blo, bhi, idesc);
+  }
+}
+// Warp-collective copy of a 128-row x 256-bit block from shared memory
+// (matrix descriptor, as for an MMA operand) into tensor memory: row i to
+// lane i, 8 columns from column t + TOFF; SOFF is added to the descriptor's
+// start-address field.  Copies run before the tcgen05.mma the same thread
+// issues after them.
+template <uint32_t TOFF, uint32_t SOFF>
+FA_DEV void tmem_cp_w(uint32_t t, uint32_t s_lo, uint32_t s_hi) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 tt, sl;\n\t.reg .b64 sd;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 tt, %0, %3;\n\t"
+      "add.u32 sl, %1, %4;\n\t"
+      "mov.b64 sd, {sl, %2};\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [tt], sd;\n\t}\n" ::"r"(t),
+      "r"(s_lo), "r"(s_hi), "n"(TOFF), "n"(SOFF)
+      : "memory");
+}
+// Copies a 128-row tile (Q or dO: K-major, 64-wide chunks 128 rows = 16 KB
+// apart, 128-byte swizzle) from shared into tensor memory, 16 features (8
+// columns, 256 bits per row) per copy: the layout the score products read
+// their A operand in (row per lane, feature pairs per column).
+template <int D, int KK>
+FA_DEV void copy_steps(uint32_t t, uint32_t slo, uint32_t shi) {
+  if constexpr (KK < D / 16) {
+    constexpr uint32_t os = ((KK >> 2) * (kBM * 128) + (KK & 3) * 32) >> 4;
+    tmem_cp_w<KK * 8, os>(t, slo, shi);
+    copy_steps<D, KK + 1>(t, slo, shi);
   }
 }
 // Unrolled K steps (64 keys in 16-wide steps) of dQ += dS K_j: A = dS in
@@ -189,8 +228,9 @@ FA_DEV RingPos ring_next(RingPos r) {
   return (r.stage + 1 == S) ? RingPos{0, r.phase ^ 1u} : RingPos{r.stage + 1, r.phase};
 }
 
-// TMA producer (one thread): per tile Q and dO into the tile's buffer, then
-// K_j, V_j through the ring.
+// TMA producer (one thread): per tile Q and dO into their buffer (once the
+// previous tile's have been copied into tensor memory), then K_j, V_j
+// through the rings.
 template <int D, bool CAUSAL, bool VARLEN>
 __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq, const CUtensorMap* tdo,
                               const CUtensorMap* tk, const CUtensorMap* tv, const DqParams& p,
@@ -204,14 +244,12 @@ __device__ void producer_role(const Shared<D, VARLEN>& sh, const CUtensorMap* tq
     for (int t = 0; t < 2; ++t) {
       const Tile x = tile_of<CAUSAL>(w, t);
       if (x.nblk == 0) continue;
-      const int qb = tit & 1;
-      if (!mbar_wait_bounded(sh.q_empty(qb), ((tit >> 1) & 1) ^ 1, sh.abort(), &g_err, kSiteProdQ, p.wait_limit_ns))
-        return;
-      mbar_arrive_expect_tx(sh.qd_full(qb), 2 * L::kTileBytes);
+      if (!mbar_wait_bounded(sh.qd_free(), (tit & 1) ^ 1, sh.abort(), &g_err, kSiteProdQ, p.wait_limit_ns)) return;
+      mbar_arrive_expect_tx(sh.qd_full(), 2 * L::kTileBytes);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sh.q_tile(qb) + c * L::kQChunk, tq, sh.qd_full(qb), c * 64, w.h, w.q_tok0 + x.row0);
-        tma_load_3d(sh.do_tile(qb) + c * L::kQChunk, tdo, sh.qd_full(qb), c * 64, w.h, w.q_tok0 + x.row0);
+        tma_load_3d(sh.q_tile() + c * L::kQChunk, tq, sh.qd_full(), c * 64, w.h, w.q_tok0 + x.row0);
+        tma_load_3d(sh.do_tile() + c * L::kQChunk, tdo, sh.qd_full(), c * 64, w.h, w.q_tok0 + x.row0);
       }
       ++tit;
       for (int j = 0; j < x.nblk; ++j) {
@@ -243,7 +281,7 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
                          const qs::PackedSched& ps, int total_units) {
   using L = Layout<D, VARLEN>;
   constexpr int kSB = L::kSB;
-  constexpr uint32_t kColDQ = kColBuf * kSB;
+  constexpr uint32_t kColDQ = L::kColDQ;
   constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);   // S, dP: 128 queries x 64 keys
   constexpr uint32_t kIdQ = idesc_bf16_f32(kBM, D, false, true);      // dQ: A in TMEM, B MN-major
   uint32_t tit = 0, sit = 0;
@@ -257,17 +295,15 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
   };
   // S and dP of global step t (the next K and V blocks of the rings) into
   // buffer t mod kSB; V_j is released as soon as its one product is issued
-  auto scores = [&](uint32_t t, int qb) -> bool {
+  auto scores = [&](uint32_t t) -> bool {
     if (!wait(sh.k_full(kr.stage), kr.phase, kSiteMmaKV)) return false;
     const int buf = t % kSB;
-    const uint64_t da = sdesc_sw128(sh.q_tile(qb), 16, 1024);
     const uint64_t dk = sdesc_sw128(sh.k_tile(kr.stage), 16, 1024);
-    score_steps<D, 0>(tmem + kColBuf * buf, desc_lo(da), desc_hi(da), desc_lo(dk), desc_hi(dk), kIdS);
+    score_steps<D, 0>(tmem + kColBuf * buf, tmem + L::kColQ, desc_lo(dk), desc_hi(dk), kIdS);
     kr = ring_next<L::kKSt>(kr);
     if (!wait(sh.v_full(vr.stage), vr.phase, kSiteMmaKV)) return false;
-    const uint64_t dg = sdesc_sw128(sh.do_tile(qb), 16, 1024);
     const uint64_t dv = sdesc_sw128(sh.v_tile(vr.stage), 16, 1024);
-    score_steps<D, 0>(tmem + kColBuf * buf + kColDPoff, desc_lo(dg), desc_hi(dg), desc_lo(dv), desc_hi(dv), kIdS);
+    score_steps<D, 0>(tmem + kColBuf * buf + kColDPoff, tmem + L::kColDO, desc_lo(dv), desc_hi(dv), kIdS);
     mma_commit_w(sh.v_empty(vr.stage));
     vr = ring_next<L::kVSt>(vr);
     mma_commit_w(sh.s_full(buf));
@@ -278,20 +314,30 @@ __device__ void mma_role(const Shared<D, VARLEN>& sh, const uint32_t tmem, const
     for (int t = 0; t < 2; ++t) {
       const Tile x = tile_of<CAUSAL>(w, t);
       if (x.nblk == 0) continue;
-      const int qb = tit & 1;
-      if (!wait(sh.qd_full(qb), (tit >> 1) & 1, kSiteMmaQ)) return;
+      // Q and dO of the tile into tensor memory, once they have landed and
+      // the previous tile's score products (the readers of the copy there)
+      // are done; the copies run before the products issued after them
+      if (!wait(sh.qd_full(), tit & 1, kSiteMmaQ)) return;
+      if (tit > 0 && !wait(sh.qd_tfree(), (tit - 1) & 1, kSiteMmaQ)) return;
+      {
+        const uint64_t dq_s = sdesc_sw128(sh.q_tile(), 16, 1024);
+        const uint64_t do_s = sdesc_sw128(sh.do_tile(), 16, 1024);
+        copy_steps<D, 0>(tmem + L::kColQ, desc_lo(dq_s), desc_hi(dq_s));
+        copy_steps<D, 0>(tmem + L::kColDO, desc_lo(do_s), desc_hi(do_s));
+        mma_commit_w(sh.qd_free());   // the shared-memory buffer may take the next tile
+      }
       // prologue: scores of the first kSB - 1 blocks
       const int pro = min(kSB - 1, x.nblk);
       for (int j = 0; j < pro; ++j)
-        if (!scores(sit + j, qb)) return;
-      if (pro == x.nblk) mma_commit_w(sh.q_empty(qb));   // every score product of the tile issued
+        if (!scores(sit + j)) return;
+      if (pro == x.nblk) mma_commit_w(sh.qd_tfree());   // every score product of the tile issued
       for (int j = 0; j < x.nblk; ++j, ++sit) {
         const int buf = sit % kSB;
         // scores kSB - 1 blocks ahead, into the buffer the previous step's
         // dQ product has just read (products run in issue order)
         if (j + kSB - 1 < x.nblk) {
-          if (!scores(sit + kSB - 1, qb)) return;
-          if (j + kSB == x.nblk) mma_commit_w(sh.q_empty(qb));
+          if (!scores(sit + kSB - 1)) return;
+          if (j + kSB == x.nblk) mma_commit_w(sh.qd_tfree());
         }
         if (!wait(sh.p_ready(buf), (sit / kSB) & 1, kSiteMmaP)) return;
         // the previous tile's dQ has been read out before this tile's first
@@ -323,7 +369,7 @@ __device__ void elementwise_role(const Shared<D, VARLEN>& sh, const uint32_t tme
   const uint64_t sl2x2 = pk2(sl2, sl2);
   __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(p.dq);
   constexpr int kSB = Layout<D, VARLEN>::kSB;
-  constexpr uint32_t kColDQ = kColBuf * kSB;
+  constexpr uint32_t kColDQ = Layout<D, VARLEN>::kColDQ;
   uint32_t tit = 0, sit = 0;
   for (int u = blockIdx.x, d = qs::first_step(p.snake); u < total_units; u += d, d = qs::next_step(d, p.snake)) {
     const qs::QUnit w = qs::decode_pair_unit<CAUSAL, VARLEN>(u, p, ps);
@@ -432,10 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   sh.base = smem;
   sh.sbase = smem_u32(smem);
   if (threadIdx.x == 0) {
-    for (int q = 0; q < 2; ++q) {
-      mbar_init(sh.qd_full(q), 1);
-      mbar_init(sh.q_empty(q), 1);
-    }
+    mbar_init(sh.qd_full(), 1);
+    mbar_init(sh.qd_free(), 1);
+    mbar_init(sh.qd_tfree(), 1);
     for (int s = 0; s < L::kKSt; ++s) {
       mbar_init(sh.k_full(s), 1);
       mbar_init(sh.k_empty(s), 1);

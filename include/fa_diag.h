@@ -106,10 +106,9 @@ FA_API fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o,
  *                   no FP32 dQ accumulator, no atomics, and the same bits on
  *                   every run.  0: one main kernel adds dQ partial sums into
  *                   the FP32 accumulator (in deterministic mode in ticket
- *                   order).  Default: 1 in deterministic mode for the dense
- *                   layout (measured faster), 0 otherwise (packed layouts:
- *                   the ticket-ordered path measured faster).  The paired
- *                   kernel ignores it.
+ *                   order).  Default: 1 in deterministic mode (measured
+ *                   faster for dense and packed layouts), 0 otherwise.  The
+ *                   paired kernel ignores it.
  * FA_ERR_INVALID_ARG for a value out of range (paired, schedule,
  * reverse_blocks, scores_first or split_dq > 1, head_group 0).
  */

@@ -34,10 +34,11 @@ def _packed(lens, Hq, Hkv, seed, D=128):
     return q, k, v, do, cu
 
 
-def _gpu(fa, q, k, v, do, cu, causal, deterministic=False):
+def _gpu(fa, q, k, v, do, cu, causal, deterministic=False, tuning=None):
     qd, kd, vd, dod, cud = (t.cuda() for t in (q, k, v, do, cu))
     o, lse = fa.fwd(qd, kd, vd, causal=causal, cu_seqlens=cud)
-    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, cu_seqlens=cud, deterministic=deterministic)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, cu_seqlens=cud, deterministic=deterministic,
+                        tuning=tuning)
     assert fa.get_device_error() == 0
     return dq.cpu(), dk.cpu(), dv.cpu()
 
@@ -105,11 +106,14 @@ def test_packed_backward_d64(fa, causal):
     _check_full(_gpu(fa, q, k, v, do, cu, causal), q, k, v, do, cu, causal)
 
 
+@pytest.mark.parametrize("tuning", [None, {"split_dq": 0}], ids=["default", "tickets"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_packed_deterministic_is_bitwise_repeatable(fa, causal):
+def test_packed_deterministic_is_bitwise_repeatable(fa, causal, tuning):
+    """Deterministic mode on packed sequences, by default (the split
+    backward) and through the ticket-ordered fused kernel."""
     q, k, v, do, cu = _packed([300, 45, 900, 128], 4, 2, seed=5)
-    a = _gpu(fa, q, k, v, do, cu, causal, deterministic=True)
-    b = _gpu(fa, q, k, v, do, cu, causal, deterministic=True)
+    a = _gpu(fa, q, k, v, do, cu, causal, deterministic=True, tuning=tuning)
+    b = _gpu(fa, q, k, v, do, cu, causal, deterministic=True, tuning=tuning)
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
     _check_full(a, q, k, v, do, cu, causal)
