@@ -73,6 +73,7 @@ struct DqParams {
   int sched_group;         // dense causal: heads per longest-first group
   int sq_pad;              // row-term floats per (batch, head) (dense) / per head (packed)
   int snake;               // deal the units boustrophedon-wise (q_sched.cuh)
+  int dq_st32;             // dQ is 32-byte aligned: its rows are written with 32-byte stores
   float scale;
   float scale_log2;
   unsigned long long wait_limit_ns;
@@ -85,7 +86,7 @@ struct Layout {
   static constexpr int kKTile = kBN * D * 2;          // K_j or V_j: 64 keys x D
   static constexpr int kKChunk = kBN * 128;           // 64 keys x 64 features (8 KB)
   static constexpr int kSB = (D == 128) ? 2 : 3;         // score buffers in tensor memory
-  static constexpr int kKSt = (D == 128) ? 4 : 6;        // K ring: blocks j .. j + kSB - 1 held, the rest loading
+  static constexpr int kKSt = (D == 128) ? 5 : 6;        // K ring: blocks j .. j + kSB - 1 held, the rest loading
   static constexpr int kVSt = (D == 128) ? 3 : 4;        // V ring
   static constexpr int kQ = 0;                                      // [Q | dO] of the next tile
   static constexpr int kK = kQ + 2 * kTileBytes;                    // [kKSt] K_j
@@ -445,14 +446,19 @@ __device__ void elementwise_role(const Shared<D, VARLEN>& sh, const uint32_t tme
           for (int e = 0; e < 32; ++e) r[e] = 0u;
         }
         if (valid) {
+          // 32 features of this row: 64 contiguous bytes, as two 32-byte
+          // stores (whole L2 sectors) when dQ allows it, else four 16-byte ones
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(r[8 * e + 0]) * p.scale, __uint_as_float(r[8 * e + 1]) * p.scale);
-            o.y = pack_bf16x2(__uint_as_float(r[8 * e + 2]) * p.scale, __uint_as_float(r[8 * e + 3]) * p.scale);
-            o.z = pack_bf16x2(__uint_as_float(r[8 * e + 4]) * p.scale, __uint_as_float(r[8 * e + 5]) * p.scale);
-            o.w = pack_bf16x2(__uint_as_float(r[8 * e + 6]) * p.scale, __uint_as_float(r[8 * e + 7]) * p.scale);
-            reinterpret_cast<uint4*>(dst + 32 * c)[e] = o;
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * p.scale, __uint_as_float(r[2 * e + 1]) * p.scale);
+          if (p.dq_st32) {
+            st_global_v8(dst + 32 * c, pk);
+            st_global_v8(dst + 32 * c + 16, pk + 8);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              reinterpret_cast<uint4*>(dst + 32 * c)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
           }
         }
       }
@@ -587,6 +593,7 @@ fa_status launch_bwd_dq(const BwdLaunch& L, cudaStream_t stream) {
   p.group = b.group;
   p.sched_group = b.B * b.Hq;   // dense causal: all heads in one longest-first group
   p.snake = (b.causal && b.cu_seqlens == nullptr && b.Sq >= 4096) ? 1 : 0;
+  p.dq_st32 = (reinterpret_cast<uintptr_t>(b.dq) & 31u) == 0;
   p.sq_pad = b.sq_pad;
   p.scale = b.scale;
   p.scale_log2 = b.scale_log2;
