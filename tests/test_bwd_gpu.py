@@ -32,10 +32,15 @@ def _inputs(B, Hq, Hkv, Sq, Sk, seed=0, q_scale=1.0, D=128):
     return q, k, v, do
 
 
-def _gpu_grads(fa, q, k, v, do, causal, deterministic=False):
+def _gpu_grads(fa, q, k, v, do, causal, deterministic=False, poison=False):
+    """poison: the gradient buffers start as NaN, so a finiteness check of
+    the result shows that every element was written."""
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
     o, lse = fa.fwd(qd, kd, vd, causal=causal)
-    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, deterministic=deterministic)
+    outs = {}
+    if poison:
+        outs = {n: torch.full_like(t, float("nan")) for n, t in (("dq", qd), ("dk", kd), ("dv", vd))}
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, deterministic=deterministic, **outs)
     assert fa.get_device_error() == 0
     return dq.cpu(), dk.cpu(), dv.cpu()
 
@@ -143,8 +148,8 @@ def test_training_shape_sampled_heads(fa, deterministic):
     """B=2, H=16, S=8192, D=128, causal: gradients of whole heads compared."""
     w = W.train(deterministic)
     (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
-    dq, dk, dv = _gpu_grads(fa, q, k, v, do, True, deterministic=deterministic)
-    for t in (dq, dk, dv):
+    dq, dk, dv = _gpu_grads(fa, q, k, v, do, True, deterministic=deterministic, poison=True)
+    for t in (dq, dk, dv):   # every element written (the buffers started as NaN)
         assert bool(torch.isfinite(t.float()).all())
     heads = [(0, 0)] if deterministic else [(0, 3), (1, 15)]
     for b, h in heads:
@@ -181,8 +186,8 @@ def test_dense_config_sampled_heads(fa, causal, stress):
     maxima in the recomputed weights."""
     w = W.dense(causal=causal, stress=stress)
     (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
-    grads = _gpu_grads(fa, q, k, v, do, causal)
-    for t in grads:
+    grads = _gpu_grads(fa, q, k, v, do, causal, poison=True)
+    for t in grads:   # every element written (the buffers started as NaN)
         assert bool(torch.isfinite(t.float()).all())
     _heads_vs_oracle(q, k, v, do, grads, causal, w.scale, [(0, 0), (1, 9), (3, 15)])
 
@@ -195,8 +200,8 @@ def test_sweep_config_sampled_heads(fa, D, S, causal):
     first and the last (batch, head) slice of each call."""
     w = W.sweep(S, D, causal)
     (q, k, v, do), _ = W.make_inputs(w, with_grad=True)
-    grads = _gpu_grads(fa, q, k, v, do, causal)
-    for t in grads:
+    grads = _gpu_grads(fa, q, k, v, do, causal, poison=True)
+    for t in grads:   # every element written (the buffers started as NaN)
         assert bool(torch.isfinite(t.float()).all())
     _heads_vs_oracle(q, k, v, do, grads, causal, w.scale, [(0, 0), (w.B - 1, 15)])
 

@@ -34,11 +34,16 @@ def _packed(lens, Hq, Hkv, seed, D=128):
     return q, k, v, do, cu
 
 
-def _gpu(fa, q, k, v, do, cu, causal, deterministic=False, tuning=None):
+def _gpu(fa, q, k, v, do, cu, causal, deterministic=False, tuning=None, poison=False):
+    """poison: the gradient buffers start as NaN (a finiteness check then
+    shows that every element was written)."""
     qd, kd, vd, dod, cud = (t.cuda() for t in (q, k, v, do, cu))
     o, lse = fa.fwd(qd, kd, vd, causal=causal, cu_seqlens=cud)
+    outs = {}
+    if poison:
+        outs = {n: torch.full_like(t, float("nan")) for n, t in (("dq", qd), ("dk", kd), ("dv", vd))}
     dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=causal, cu_seqlens=cud, deterministic=deterministic,
-                        tuning=tuning)
+                        tuning=tuning, **outs)
     assert fa.get_device_error() == 0
     return dq.cpu(), dk.cpu(), dv.cpu()
 
@@ -155,13 +160,15 @@ def test_packed_matches_dense_for_equal_lengths(fa):
         assert rel_fro(f64(x), f64(y.cpu().view(B * S, H, 128))) <= 2e-3
 
 
-def test_varlen_gqa_config_sampled_sequences(fa):
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_varlen_gqa_config_sampled_sequences(fa, deterministic):
     """64 packed sequences (lengths 128..8192), Hq=32, Hkv=8, causal: whole
-    (sequence, head) gradients of a few sequences compared with the oracle."""
+    (sequence, head) gradients of a few sequences compared with the oracle,
+    atomic and deterministic (the split backward)."""
     w = W.varlen_gqa()
     (q, k, v, do), cu = W.make_inputs(w, with_grad=True)
-    dq, dk, dv = _gpu(fa, q, k, v, do, cu, True)
-    for t in (dq, dk, dv):
+    dq, dk, dv = _gpu(fa, q, k, v, do, cu, True, deterministic=deterministic, poison=True)
+    for t in (dq, dk, dv):   # every element written (the buffers started as NaN)
         assert bool(torch.isfinite(t.float()).all())
     lens = np.diff(cu.numpy())
     seqs = [int(np.argmin(lens)), int(np.argmax(lens)), 17]
