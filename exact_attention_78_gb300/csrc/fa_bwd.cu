@@ -19,9 +19,14 @@
 //         per unit, so they need no atomics.  dQ partial sums are added by the
 //         TMA unit (bulk tensor reduce-adds of 32 x D FP32 tiles staged
 //         through two shared-memory buffers, so one tile is written while the
-//         other is read), in deterministic mode in ascending key-block order
-//         enforced by one ticket per (batch, head, query block);
+//         other is read), in deterministic mode (when selected instead of
+//         the split backward below) in ascending key-block order enforced by
+//         one ticket per (batch, head, query block);
 //   post  dQ = BF16(scale * accumulator).
+//
+// Deterministic mode runs by default as a split backward: this main kernel
+// without its dQ product (dK, dV only; no accumulator, no post pass), and the
+// dQ kernel of fa_bwd_dq.cu, which computes each dQ tile whole.
 //
 // Sources: "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for
 // Asymmetric Hardware Scaling" (fdeinterviews.com summary): the paragraph on

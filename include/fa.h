@@ -113,15 +113,18 @@ FA_API size_t fa_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int 
  * inputs, its outputs O and LSE, and the upstream gradient dO, writes dQ, dK,
  * dV (BF16; dK/dV of a key/value head sum over its query-head group).
  *   deterministic  0: dQ partial sums are added with FP32 atomics (order may
- *                  vary run to run); 1: they are added in a fixed order so
- *                  repeated calls give bitwise-identical dQ.
+ *                  vary run to run); 1: dQ is summed over the key blocks in
+ *                  a fixed order, so repeated calls give bitwise-identical
+ *                  dQ (by default a second main kernel computes each dQ
+ *                  tile whole in tensor memory; fa_bwd_ex can select
+ *                  ticket-ordered additions in the fused kernel instead).
  *   workspace      device, 256-byte aligned, at least
  *                  fa_bwd_workspace_size(...) bytes (for the packed layout
  *                  sized with total_q = Sq); contents on entry are ignored
  *                  and clobbered.
  * Head dimension 64 or 128, like fa_fwd().
- * Launches three kernels on `stream` (row terms, main pass, dQ conversion),
- * four for the packed layout (a first one checks the offsets and builds the
+ * Launches three kernels on `stream` (row terms, main pass, dQ conversion; in
+ * deterministic mode the last is the dQ kernel), four for the packed layout (a first one checks the offsets and builds the
  * per-sequence tables).
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
