@@ -225,6 +225,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float*
     L.v = v;
     L.p.o = o;
     L.p.lse = lse;
+    L.p.o_st32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     L.p.cu_seqlens = cu_seqlens;
     L.p.B = B;
     L.p.Hq = Hq;

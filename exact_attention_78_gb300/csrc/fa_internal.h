@@ -28,6 +28,7 @@ struct FwdParams {
   int split_p;             // 1: each half of P (64 keys) is signalled to the MMA warp on its own
   int sched_group;         // dense causal: (batch, head) pairs per group of the longest-first unit order
   int snake;               // deal the units over the grid boustrophedon-wise (q_sched.cuh)
+  int o_st32;              // O is 32-byte aligned: its rows are written with 32-byte stores
   unsigned long long wait_limit_ns;
 };
 

@@ -84,3 +84,19 @@ def test_gradients_into_16_byte_aligned_buffers(fa, D):
     assert fa.get_device_error() == 0
     for a, b in zip(ref, got):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_output_into_16_byte_aligned_buffer(fa, D, causal):
+    """O rows are written with 32-byte stores when O is 32-byte aligned and
+    with 16-byte stores otherwise (the ABI asks for 16): same bits."""
+    q, k, v, _ = _qkv(B=2, H=2, S=300, D=D)
+    ref_o, ref_l = fa.fwd(q, k, v, causal=causal)
+    buf = torch.empty(q.numel() + 8, dtype=q.dtype, device=q.device)
+    o = buf[8:].view(q.shape)                  # 16 bytes past a 512-byte-aligned allocation
+    assert o.data_ptr() % 32 == 16
+    got_o, got_l = fa.fwd(q, k, v, causal=causal, out=o)
+    assert fa.get_device_error() == 0
+    assert torch.equal(ref_o.view(torch.int16), got_o.view(torch.int16))
+    assert torch.equal(ref_l, got_l)
