@@ -55,8 +55,9 @@ constexpr int kSchedBytes = 4 * kSchedInts;
 // load (training shape B = 2, S = 8192: 14%), against 0-2% for this order
 // (computed over the sweep's unit costs).  Measured on GB300 (forward,
 // same box): causal B=4 S=4096 +4%, training shape B=2 S=8192 +6%, S=32768
-// +6%, but S=1024 (B=32) -3.5%; so the host asks for it (`snake`) for dense
-// causal calls with S >= 4096 only, and otherwise every step is G.
+// +6%, but S=1024 (B=32) -3.5% and S=2048 (B=16) -1.1%; so the host asks
+// for it (`snake`) for dense causal calls with S >= 4096 only, and otherwise
+// every step is G.
 FA_DEV int first_step(bool snake) { return snake ? 2 * (int)(gridDim.x - 1 - blockIdx.x) + 1 : (int)gridDim.x; }
 FA_DEV int next_step(int d, bool snake) { return snake ? 2 * (int)gridDim.x - d : d; }
 
